@@ -1,0 +1,192 @@
+"""Seeded synthetic inputs for the prefill path.
+
+This module only draws random numbers and lays out ragged-batch metadata; it
+holds none of the attention arithmetic, so both the CUDA path's tests and the
+oracle can take their inputs from it.
+
+Distributions follow the workloads the pages describe for gpt-oss-shaped
+layers (hip-ep PR #622 sink/window harness: H=64, G=8, d=64, pure and chunked
+prefill over past lengths 512/8192; SGLang PR #34468 microbench: prefix /
+extend pairs, window 128, full and window-bounded prefix layouts): Q, K, V are
+drawn i.i.d. N(0, 1) in fp32 and rounded to the 16-bit input type; per-head
+sink logits are N(0, 1), rounded to the input type and handed over as fp32.
+There are no model weights: these tensors stand in for a real model's
+activations.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import List, Optional
+
+import torch
+
+DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+@dataclass
+class Batch:
+    """One call's inputs, on the CPU unless moved with :meth:`to`."""
+    q: torch.Tensor              # [total_q, hq, d]
+    k: torch.Tensor              # [total_kv, hkv, d]
+    v: torch.Tensor              # [total_kv, hkv, d]
+    cu_seqlens_q: torch.Tensor   # int32 [B+1]
+    prefix_lens: torch.Tensor    # int32 [B]
+    kv_indptr: torch.Tensor      # int32 [B+1]
+    hq: int
+    hkv: int
+    d: int
+    window: int                  # <= 0: none
+    sinks: Optional[torch.Tensor]  # fp32 [hq] or None
+    smooth: bool
+    scale: float
+    name: str = ""
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.prefix_lens.numel())
+
+    @property
+    def total_q(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def total_kv(self) -> int:
+        return int(self.k.shape[0])
+
+    @property
+    def max_seqlen_q(self) -> int:
+        e = self.extend_lens
+        return max(e) if e else 0
+
+    @property
+    def extend_lens(self) -> List[int]:
+        cu = self.cu_seqlens_q.tolist()
+        return [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
+
+    @property
+    def dtype_name(self) -> str:
+        return "bf16" if self.q.dtype == torch.bfloat16 else "f16"
+
+    def to(self, device) -> "Batch":
+        mv = lambda t: None if t is None else t.to(device)
+        return Batch(mv(self.q), mv(self.k), mv(self.v), mv(self.cu_seqlens_q),
+                     mv(self.prefix_lens), mv(self.kv_indptr), self.hq, self.hkv,
+                     self.d, self.window, mv(self.sinks), self.smooth, self.scale,
+                     self.name, dict(self.meta))
+
+
+def _normal(gen, shape, dtype):
+    return torch.randn(*shape, generator=gen, dtype=torch.float32).to(dtype)
+
+
+def make_batch(prefix_lens, extend_lens, hq, hkv, d, dtype="bf16", window=0,
+               sink_mode="head", seed=0, scale=None, name="") -> Batch:
+    """Ragged batch: sequence b has prefix_lens[b] cached keys followed by
+    extend_lens[b] new tokens; its KV rows are packed [prefix | extend] back to
+    back in sequence order.  sink_mode is "none", "head" or "smooth"."""
+    assert len(prefix_lens) == len(extend_lens)
+    dt = DTYPES[dtype] if isinstance(dtype, str) else dtype
+    gen = torch.Generator().manual_seed(int(seed))
+    b = len(prefix_lens)
+    cu = [0]
+    kvp = [0]
+    for p, e in zip(prefix_lens, extend_lens):
+        cu.append(cu[-1] + int(e))
+        kvp.append(kvp[-1] + int(p) + int(e))
+    total_q, total_kv = cu[-1], kvp[-1]
+    q = _normal(gen, (total_q, hq, d), dt)
+    k = _normal(gen, (total_kv, hkv, d), dt)
+    v = _normal(gen, (total_kv, hkv, d), dt)
+    sinks = None
+    if sink_mode == "head":
+        sinks = _normal(gen, (hq,), dt).to(torch.float32)
+    elif sink_mode not in ("none", "smooth"):
+        raise ValueError(sink_mode)
+    return Batch(q, k, v,
+                 torch.tensor(cu, dtype=torch.int32),
+                 torch.tensor([int(p) for p in prefix_lens], dtype=torch.int32),
+                 torch.tensor(kvp, dtype=torch.int32),
+                 hq, hkv, d, int(window), sinks, sink_mode == "smooth",
+                 float(scale if scale is not None else d ** -0.5), name,
+                 {"seed": int(seed), "num_seqs": b})
+
+
+def window_bounded(batch: Batch, window: int) -> Batch:
+    """The same batch with each sequence's prefix cut to its last
+    min(prefix, window) rows, the layout a serving stack hands a
+    sliding-window layer (SGLang PR #34468, commit 1: window_kv_indptr).
+    Positions inside the kernel are relative, so the result must not change."""
+    cu = batch.cu_seqlens_q.tolist()
+    kvp = batch.kv_indptr.tolist()
+    pre = batch.prefix_lens.tolist()
+    ks, vs, new_pre, new_kvp = [], [], [], [0]
+    for i, p in enumerate(pre):
+        e = cu[i + 1] - cu[i]
+        keep = min(p, window) if window > 0 else p
+        lo = kvp[i] + (p - keep)
+        ks.append(batch.k[lo:kvp[i + 1]])
+        vs.append(batch.v[lo:kvp[i + 1]])
+        new_pre.append(keep)
+        new_kvp.append(new_kvp[-1] + keep + e)
+    return Batch(batch.q, torch.cat(ks), torch.cat(vs), batch.cu_seqlens_q,
+                 torch.tensor(new_pre, dtype=torch.int32),
+                 torch.tensor(new_kvp, dtype=torch.int32), batch.hq, batch.hkv,
+                 batch.d, batch.window, batch.sinks, batch.smooth, batch.scale,
+                 batch.name + "/window-bounded", dict(batch.meta))
+
+
+# ---------------------------------------------------------------- named sets
+
+def tiny(seed: int = 0) -> Batch:
+    """Single sequence, 256 tokens, no prefix, Hq=4 / Hkv=1, d=64, fp16,
+    window 32, per-head sinks."""
+    return make_batch([0], [256], 4, 1, 64, "f16", window=32, sink_mode="head",
+                      seed=seed, name="tiny-w32")
+
+
+def layer_pair(seq: int = 4096, seed: int = 1) -> List[Batch]:
+    """gpt-oss layer pair, pure prefill: one full-causal and one window-128
+    layer at Hq=64 / Hkv=8, d=64, bf16, per-head sinks."""
+    full = make_batch([0], [seq], 64, 8, 64, "bf16", window=0,
+                      sink_mode="head", seed=seed, name=f"pair-full-s{seq}")
+    win = make_batch([0], [seq], 64, 8, 64, "bf16", window=128,
+                     sink_mode="head", seed=seed + 100, name=f"pair-w128-s{seq}")
+    return [full, win]
+
+
+def chunked_prefix(num_seqs: int = 8, prefix: int = 8192, extend: int = 8192,
+                   window: int = 128, seed: int = 2) -> Batch:
+    """Chunked prefill over a cached prefix, full-prefix KV layout; pass the
+    result through window_bounded() for the min(prefix, window) layout."""
+    return make_batch([prefix] * num_seqs, [extend] * num_seqs, 64, 8, 64,
+                      "bf16", window=window, sink_mode="head", seed=seed,
+                      name=f"chunked-p{prefix}-e{extend}x{num_seqs}-w{window}")
+
+
+def oss20b_chunk(layer: int, chunk: int, chunk_len: int = 512,
+                 seed: int = 3) -> Batch:
+    """One call of a gpt-oss-20b-like 16k prefill processed in chunks of 512:
+    layer parity picks full-causal (even) or window-128 (odd); the prefix is
+    the chunk_len * chunk tokens already processed."""
+    window = 0 if layer % 2 == 0 else 128
+    return make_batch([chunk_len * chunk], [chunk_len], 64, 8, 64, "bf16",
+                      window=window, sink_mode="head",
+                      seed=seed * 100003 + layer * 1009 + chunk,
+                      name=f"oss20b-L{layer}-c{chunk}")
+
+
+RAGGED_WINDOWS = [1, 15, 64, 127, 128, 129, 4096, 0]
+
+
+def ragged(num_seqs: int = 16, max_prefix: int = 16384, max_extend: int = 8192,
+           hq: int = 64, hkv: int = 8, d: int = 64, dtype: str = "bf16",
+           window: int = 0, sink_mode: str = "head", seed: int = 4) -> Batch:
+    """Ragged varlen batch: prefixes uniform in [0, max_prefix], extends
+    uniform in [1, max_extend], drawn once per seed."""
+    gen = torch.Generator().manual_seed(int(seed) * 7919 + 17)
+    pre = torch.randint(0, max_prefix + 1, (num_seqs,), generator=gen).tolist()
+    ext = torch.randint(1, max_extend + 1, (num_seqs,), generator=gen).tolist()
+    return make_batch(pre, ext, hq, hkv, d, dtype, window=window,
+                      sink_mode=sink_mode, seed=seed,
+                      name=f"ragged-{num_seqs}-h{hq}/{hkv}-d{d}-{dtype}-w{window}-{sink_mode}")
