@@ -1,0 +1,398 @@
+"""Benchmark of the fused GQA flash-attention prefill on one GB300.
+
+Workload (one "step"): a gpt-oss layer pair in pure prefill -- batch 1, 4096
+tokens, Hq=64 / Hkv=8, d=64, bf16 Q/K/V ~ N(0,1) (synthetic: no model
+weights), per-head sinks ~ N(0,1), one full-causal layer and one window-128
+layer.  Both layers' inputs are resident in HBM before timing starts.
+
+Metric: useful attention TFLOP/s = 4 * d * Hq * (unmasked query-key pairs) /
+time, counting only pairs the mask keeps; also prefill tokens/s and the
+fraction of the measured dense bf16 tensor peak.
+
+Between timed steps a 256 MiB buffer is written to flush the 126 MB L2; each
+step is timed alone with CUDA events on the launching stream, so the flush is
+outside the measured time.  `--impl reference` times the CPU oracle instead
+(on a bounded sample of rows of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "useful attention TFLOP/s & prefill tok/s at 1 GB300; % of bf16 tensor peak"
+UNIT = "TFLOP/s"
+WORKLOAD = "gpt-oss layer pair, pure prefill: B=1, seq 4096, Hq=64, Hkv=8, d=64, bf16, full-causal + window-128, per-head sinks"
+
+
+def useful_pairs(prefix_lens, extend_lens, window):
+    """Unmasked (query, key) pairs per head: sum over rows of the keys the
+    causal / window mask keeps."""
+    total = 0
+    for p, e in zip(prefix_lens, extend_lens):
+        for i in range(e):
+            n = p + i + 1
+            total += min(n, window) if window > 0 else n
+    return total
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return {"bf16_tflops": pk["bf16_tflops"], "bf16_tflops_sustained": pk["bf16_tflops_sustained"],
+                "hbm_gbs": pk["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+            "source": "fallback"}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gqa_flash_attention_prefill_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the full-causal kernel from the committed ncu
+    summary, or None when the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return rec.get("full_layer_dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[2:]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    """One process per GPU under torchrun: each rank runs its own replica of
+    the workload (the layer pair shards with no exchange step); returns
+    (rank, world)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("GQA_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend)
+    return rank, world
+
+
+def dist_max(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_ours(args, rank, world):
+    import torch
+    import gqa_flash_attention_prefill_gb300 as pkg
+    from gqa_flash_attention_prefill_gb300 import workloads as W
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    pkg.load()
+    layers_cpu = W.layer_pair(seq=args.seq, seed=1)
+    layers = [b.to("cuda") for b in layers_cpu]
+    outs = [torch.empty_like(b.q) for b in layers]
+    lses = [torch.empty(b.q.shape[:2], dtype=torch.float32, device="cuda") for b in layers]
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+
+    def step():
+        for b, o, l in zip(layers, outs, lses):
+            pkg.prefill(b, out=o, lse=l, stream=stream)
+
+    pairs = [useful_pairs(b.prefix_lens.tolist(), b.extend_lens, b.window) for b in layers]
+    flops = [4.0 * b.d * b.hq * n for b, n in zip(layers, pairs)]
+    tokens = sum(b.total_q for b in layers)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if pkg.get_device_status() != 0:
+        raise RuntimeError("device status word raised during warm-up")
+
+    # Timed region: per step, flush L2 (untimed), then time each layer's
+    # launch with events on the launching stream.
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            pkg.prefill(layers[0], out=outs[0], lse=lses[0], stream=stream)
+            ev[i][1].record(stream)
+            pkg.prefill(layers[1], out=outs[1], lse=lses[1], stream=stream)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        t_wall1 = time.perf_counter()
+    dist_barrier(world)
+    t_full = [e[0].elapsed_time(e[1]) for e in ev]
+    t_win = [e[1].elapsed_time(e[2]) for e in ev]
+    ms_step = statistics.mean(a + b for a, b in zip(t_full, t_win))
+    ms_step = dist_max(ms_step, world)
+    if pkg.get_device_status() != 0:
+        raise RuntimeError("device status word raised during the timed region")
+
+    peaks = load_peaks()
+    value = world * sum(flops) / (ms_step * 1e-3) / 1e12
+    full_ms = statistics.mean(t_full)
+    achieved = flops[0] / (full_ms * 1e-3) / 1e12
+
+    # End to end through the C ABI from pinned host buffers: per step, copy
+    # this step's inputs host->device, run both layers, read the outputs back.
+    host = []
+    for b in layers_cpu:
+        hb = {n: getattr(b, n).pin_memory() for n in ("q", "k", "v", "cu_seqlens_q",
+                                                       "prefix_lens", "kv_indptr", "sinks")}
+        host.append(hb)
+    host_out = [torch.empty(b.q.shape, dtype=b.q.dtype).pin_memory() for b in layers_cpu]
+    host_lse = [torch.empty(b.q.shape[:2], dtype=torch.float32).pin_memory() for b in layers_cpu]
+    h2d = sum(t.numel() * t.element_size() for hb in host for t in hb.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out + host_lse)
+
+    def e2e_step():
+        for hb, b, o, l, ho, hl in zip(host, layers, outs, lses, host_out, host_lse):
+            for n, t in hb.items():
+                getattr(b, n).copy_(t, non_blocking=True)
+            pkg.prefill(b, out=o, lse=l, stream=stream)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(l, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = dist_max(e0.elapsed_time(e1) / e2e_steps, world)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) Q/K/V and sinks; no model weights)",
+        "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": args.seq,
+                   "layers": ["full-causal", "window-128"], "l2": "flushed between steps (256 MiB write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tokens_per_s": round(world * tokens / 2 / (ms_step * 1e-3), 1),
+        "pct_of_bf16_peak": round(100.0 * value / (world * peaks["bf16_tflops"]), 2),
+        "per_layer_ms": {"full_causal": round(full_ms, 5),
+                         "window_128": round(statistics.mean(t_win), 5)},
+        "per_layer_tflops": {"full_causal": round(achieved, 2),
+                             "window_128": round(flops[1] / (statistics.mean(t_win) * 1e-3) / 1e12, 2)},
+        "roofline": {"bound": "tensor", "kernel": "prefill_kernel<64,128,...,full-causal>",
+                     "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                     "traffic": recorded_traffic(), "peak_source": peaks["source"] + " burst bf16"},
+        "e2e": {"value": round(world * sum(flops) / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+        "timed_wall_s": round(t_wall1 - t_wall0, 3),
+    }
+    return line
+
+
+def oracle_sample_run(layers_cpu, rows_per_layer, offset=0):
+    """Runs the CPU oracle on `rows_per_layer` evenly spaced query rows of
+    each layer; returns (seconds, useful flops, rows)."""
+    import numpy as np
+    import oracle
+    total_s, total_flops, total_rows = 0.0, 0.0, 0
+    for b in layers_cpu:
+        e = b.total_q
+        step = max(1, e // rows_per_layer)
+        rows = (np.arange(rows_per_layer) * step + offset) % e
+        t0 = time.perf_counter()
+        oracle.prefill(b.q, b.k, b.v, b.cu_seqlens_q, b.prefix_lens, b.kv_indptr,
+                       b.scale, b.window, sinks=b.sinks, smooth_softmax=b.smooth, rows=rows)
+        total_s += time.perf_counter() - t0
+        pre = int(b.prefix_lens[0])
+        for r in rows:
+            n = pre + int(r) + 1
+            total_flops += 4.0 * b.d * b.hq * (min(n, b.window) if b.window > 0 else n)
+        total_rows += len(rows)
+    return total_s, total_flops, total_rows
+
+
+def size_oracle_sample(layers_cpu, target_s):
+    """Rows per layer so that one oracle sample takes about target_s."""
+    probe = 32
+    t, _, _ = oracle_sample_run(layers_cpu, probe)
+    per_row = max(t / probe, 1e-6)
+    return int(max(8, min(layers_cpu[0].total_q, target_s / per_row)))
+
+
+def cpu_baseline(args):
+    import oracle
+    from gqa_flash_attention_prefill_gb300 import workloads as W
+    oracle.build()
+    layers_cpu = W.layer_pair(seq=args.seq, seed=1)
+    rows = size_oracle_sample(layers_cpu, args.cpu_seconds)
+    t, fl, n = oracle_sample_run(layers_cpu, rows)
+    return {"value": fl / t / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{rows} evenly spaced query rows of each layer (of {layers_cpu[0].total_q}), "
+                      f"all {layers_cpu[0].hq} heads; {n} rows in {t:.1f} s; "
+                      f"tokens/s {n / t:.1f}"}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm, on this workload's metric."""
+    if rank != 0:
+        return None
+    import oracle
+    from gqa_flash_attention_prefill_gb300 import workloads as W
+    oracle.build()
+    layers_cpu = W.layer_pair(seq=args.seq, seed=1)
+    per_step_s = max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    rows = size_oracle_sample(layers_cpu, per_step_s)
+    for i in range(args.warmup):
+        oracle_sample_run(layers_cpu, rows, offset=i)
+    secs, fl_total = 0.0, 0.0
+    for i in range(args.steps):
+        t, fl, n = oracle_sample_run(layers_cpu, rows, offset=args.warmup + i)
+        secs += t
+        fl_total += fl
+    value = fl_total / secs / 1e12
+    cores = oracle.num_threads()
+    sample = (f"each step: {rows} evenly spaced query rows of each layer (of "
+              f"{layers_cpu[0].total_q}), all {layers_cpu[0].hq} heads, fp64 CPU oracle")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) Q/K/V and sinks; no model weights)",
+            "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": args.seq,
+                       "layers": ["full-causal", "window-128"]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seq", type=int, default=4096)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="CPU work of the oracle baseline sample (rank 0, N=1)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world)
+        if rank == 0:
+            if world == 1 and not args.no_cpu_baseline:
+                line["cpu_baseline"] = cpu_baseline(args)
+            else:
+                line["cpu_baseline"] = None
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

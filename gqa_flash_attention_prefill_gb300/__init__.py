@@ -1,0 +1,196 @@
+"""Fused GQA flash-attention prefill for GB300 (sm_103a).
+
+Thin ctypes binding over ``libgqa_prefill.so`` (the C ABI declared in
+``include/gqa_prefill.h``): the functions here only marshal torch tensors into
+pointers and sizes.  Every step of the computation runs in the CUDA kernels;
+there is no CPU or PyTorch fallback, and calling in without the built library
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+__all__ = ["load", "gqa_flash_prefill", "gqa_flash_prefill_debug", "prefill",
+           "plan", "force_block_n", "get_device_status", "GQAError",
+           "GQA_F16", "GQA_BF16", "GQA_DEV_TIMEOUT", "GQA_DEV_BAD_METADATA",
+           "EXPORTED_SYMBOLS"]
+
+GQA_F16, GQA_BF16 = 0, 1
+GQA_OK, GQA_ERR_INVALID, GQA_ERR_UNSUPPORTED, GQA_ERR_CUDA = 0, -1, -2, -3
+GQA_DEV_TIMEOUT, GQA_DEV_BAD_METADATA = 1, 2
+
+EXPORTED_SYMBOLS = [
+    "gqa_flash_prefill", "gqa_flash_prefill_debug", "gqa_prefill_plan",
+    "gqa_prefill_force_block_n", "gqa_prefill_get_device_status",
+    "gqa_prefill_status_string", "gqa_prefill_version",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgqa_prefill.so")
+_lib = None
+
+
+class GQAError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {code} ({_status_string(code)})")
+
+
+class _Plan(ctypes.Structure):
+    _fields_ = [("rows_per_unit", ctypes.c_int), ("block_n", ctypes.c_int),
+                ("kv_stages", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
+                ("grid", ctypes.c_int), ("max_units", ctypes.c_int)]
+
+
+def load(path: Optional[str] = None):
+    """Load libgqa_prefill.so (built by ``__graft_entry__.build()`` or
+    ``python -m gqa_flash_attention_prefill_gb300.build``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"CUDA library {p} is missing: build it with "
+            "`python -m gqa_flash_attention_prefill_gb300.build`")
+    lib = ctypes.CDLL(p)
+    vp, i32p, fp = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+    core = [vp, vp, vp, i32p, i32p, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_float, ctypes.c_int, fp, ctypes.c_int, vp, fp, vp]
+    lib.gqa_flash_prefill.argtypes = core
+    lib.gqa_flash_prefill.restype = ctypes.c_int
+    lib.gqa_flash_prefill_debug.argtypes = core + [vp]
+    lib.gqa_flash_prefill_debug.restype = ctypes.c_int
+    lib.gqa_prefill_plan.argtypes = [ctypes.c_int] * 8 + [ctypes.POINTER(_Plan)]
+    lib.gqa_prefill_plan.restype = ctypes.c_int
+    lib.gqa_prefill_force_block_n.argtypes = [ctypes.c_int]
+    lib.gqa_prefill_force_block_n.restype = ctypes.c_int
+    lib.gqa_prefill_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    lib.gqa_prefill_get_device_status.restype = ctypes.c_int
+    lib.gqa_prefill_status_string.argtypes = [ctypes.c_int]
+    lib.gqa_prefill_status_string.restype = ctypes.c_char_p
+    lib.gqa_prefill_version.argtypes = []
+    lib.gqa_prefill_version.restype = ctypes.c_char_p
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _status_string(code: int) -> str:
+    try:
+        return load().gqa_prefill_status_string(code).decode()
+    except Exception:  # pragma: no cover - library missing
+        return "?"
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return GQA_BF16
+    if t.dtype == torch.float16:
+        return GQA_F16
+    raise TypeError(f"q/k/v must be float16 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _args(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, scale, window, sinks,
+          smooth_softmax, out, lse, stream, max_seqlen_q):
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if t.dim() != 3 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [rows, heads, d] tensor")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("prefix_lens", prefix_lens),
+                    ("kv_indptr", kv_indptr)):
+        if str(t.dtype) != "torch.int32" or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 tensor")
+    total_q, hq, d = q.shape
+    total_kv, hkv, _ = k.shape
+    return (_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(prefix_lens),
+            _ptr(kv_indptr), int(prefix_lens.numel()), int(total_q), int(total_kv),
+            int(max_seqlen_q), int(hq), int(hkv), int(d), _dtype_code(q), float(scale),
+            int(window), _ptr(sinks), 1 if smooth_softmax else 0, _ptr(out), _ptr(lse),
+            _stream_handle(stream))
+
+
+def gqa_flash_prefill(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, scale,
+                      window=0, sinks=None, smooth_softmax=False, out=None,
+                      lse=None, stream=None, max_seqlen_q=0):
+    """Marshal torch CUDA tensors into the C ABI call (see gqa_prefill.h).
+    ``out`` [total_q, Hq, d] and ``lse`` (fp32 [total_q, Hq] or None) are
+    written in place; returns ``out``."""
+    rc = load().gqa_flash_prefill(*_args(q, k, v, cu_seqlens_q, prefix_lens,
+                                         kv_indptr, scale, window, sinks,
+                                         smooth_softmax, out, lse, stream,
+                                         max_seqlen_q))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_flash_prefill")
+    return out
+
+
+def gqa_flash_prefill_debug(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, scale,
+                            unit_log, window=0, sinks=None, smooth_softmax=False,
+                            out=None, lse=None, stream=None, max_seqlen_q=0):
+    """Same as gqa_flash_prefill, and writes one 8-int record per work unit
+    into ``unit_log`` (device int32 [max_units, 8])."""
+    rc = load().gqa_flash_prefill_debug(*_args(q, k, v, cu_seqlens_q, prefix_lens,
+                                               kv_indptr, scale, window, sinks,
+                                               smooth_softmax, out, lse, stream,
+                                               max_seqlen_q), _ptr(unit_log))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_flash_prefill_debug")
+    return out
+
+
+def prefill(batch, out=None, lse=None, with_lse=True, stream=None):
+    """Run one ``workloads.Batch`` already on the GPU; allocates out/lse with
+    torch when not given.  Returns (out, lse)."""
+    import torch
+    if out is None:
+        out = torch.empty_like(batch.q)
+    if lse is None and with_lse:
+        lse = torch.empty(batch.q.shape[:2], dtype=torch.float32, device=batch.q.device)
+    gqa_flash_prefill(batch.q, batch.k, batch.v, batch.cu_seqlens_q,
+                      batch.prefix_lens, batch.kv_indptr, batch.scale,
+                      window=batch.window, sinks=batch.sinks,
+                      smooth_softmax=batch.smooth, out=out, lse=lse,
+                      stream=stream, max_seqlen_q=batch.max_seqlen_q)
+    return out, lse
+
+
+def plan(num_seqs, total_q, max_seqlen_q, hq, hkv, d, dtype, window) -> dict:
+    """Host-only launch plan (rows_per_unit, block_n, kv_stages, ctas_per_sm,
+    grid, max_units) for a call with these shapes."""
+    p = _Plan()
+    code = dtype if isinstance(dtype, int) else (GQA_BF16 if "bf16" in str(dtype) else GQA_F16)
+    rc = load().gqa_prefill_plan(int(num_seqs), int(total_q), int(max_seqlen_q), int(hq),
+                                 int(hkv), int(d), code, int(window), ctypes.byref(p))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_prefill_plan")
+    return {f: getattr(p, f) for f, _ in _Plan._fields_}
+
+
+def force_block_n(block_n: int) -> None:
+    rc = load().gqa_prefill_force_block_n(int(block_n))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_prefill_force_block_n")
+
+
+def get_device_status() -> int:
+    """Read and clear the device status word (synchronises the device)."""
+    v = ctypes.c_int(0)
+    rc = load().gqa_prefill_get_device_status(ctypes.byref(v))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_prefill_get_device_status")
+    return v.value

@@ -1,0 +1,342 @@
+// host.cu -- C ABI of libgqa_prefill.so: argument validation, the launch
+// configuration cache, TMA tensor maps and the launch.  Declared in
+// include/gqa_prefill.h, which states the operation, layouts and errors.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "../../include/gqa_prefill.h"
+#include "launch.h"
+
+namespace gqa {
+
+// Device status word (GQA_DEV_* bits); kernels receive its address.
+__device__ unsigned int g_device_status;
+
+namespace {
+
+std::mutex g_mu;      // guards the configuration cache and the forced tile size
+std::mutex g_dev_mu;  // guards the per-device information
+int g_forced_block_n = 0;
+
+struct DeviceInfo {
+  int sms = 0;
+  int smem_per_sm = 0;
+  unsigned int* status = nullptr;
+};
+std::map<int, DeviceInfo> g_devices;
+
+// Launch-configuration cache.  Keyed on what changes which tile shape wins
+// (head dim, a power-of-two bucket of the query length, heads, group size,
+// windowed or not, dtype) and never on the KV length: the KV length only
+// scales every candidate's loop uniformly (hip-ep PR #622, config-cache
+// commit), while a window caps the tiles walked and so may change the winner
+// (same page, window commit).
+using CfgKey = std::tuple<int, int, int, int, int, int>;
+std::map<CfgKey, int> g_cfg_cache;
+
+bool env_flag(const char* name) {
+  const char* v = std::getenv(name);
+  return v != nullptr && v[0] != '\0' && v[0] != '0';
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+int device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  auto itr = g_devices.find(dev);
+  if (itr == g_devices.end()) {
+    DeviceInfo di;
+    if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return GQA_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                               dev) != cudaSuccess)
+      return GQA_ERR_CUDA;
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return GQA_ERR_CUDA;
+    di.status = static_cast<unsigned int*>(ptr);
+    itr = g_devices.emplace(dev, di).first;
+  }
+  *out = itr->second;
+  return GQA_OK;
+}
+
+int pow2_bucket(int x) {
+  int b = 1;
+  while (b < x && b < (1 << 30)) b <<= 1;
+  return b;
+}
+
+int default_block_n(int d, bool windowed) {
+  (void)windowed;
+  if (d == 64) return 128;
+  return 64;
+}
+
+struct Plan {
+  KernelShape shape;
+  int rows, G, ctas_per_sm, grid, max_units;
+  unsigned smem_launch;  // dynamic smem requested per CTA
+};
+
+int make_plan(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, int d, int dtype,
+              int window, Plan* pl) {
+  if (num_seqs < 0 || total_q < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0)
+    return GQA_ERR_INVALID;
+  if (dtype != GQA_F16 && dtype != GQA_BF16) return GQA_ERR_INVALID;
+  if (d != 64 && d != 128 && d != 256) return GQA_ERR_UNSUPPORTED;
+  const int G = Hq / Hkv;
+  if (G > 128 || 128 % G != 0) return GQA_ERR_UNSUPPORTED;
+  if (num_seqs > kMaxSeqs) return GQA_ERR_UNSUPPORTED;
+  DeviceInfo di;
+  const bool have_dev = device_info(&di) == GQA_OK;
+  int bn;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_forced_block_n != 0) {
+      bn = g_forced_block_n;
+    } else {
+      const CfgKey key{d, pow2_bucket(max_seqlen_q > 0 ? max_seqlen_q : total_q), Hq, G,
+                       window > 0 ? 1 : 0, dtype};
+      auto itr = g_cfg_cache.find(key);
+      if (itr == g_cfg_cache.end())
+        itr = g_cfg_cache.emplace(key, default_block_n(d, window > 0)).first;
+      bn = itr->second;
+    }
+  }
+  if (!kernel_shape(d, bn, &pl->shape)) return GQA_ERR_UNSUPPORTED;
+  pl->G = G;
+  pl->rows = 128 / G;
+  const long long max_units =
+      (long long)Hkv * ((total_q + pl->rows - 1) / pl->rows + (long long)num_seqs);
+  if (max_units > (1ll << 30)) return GQA_ERR_UNSUPPORTED;
+  pl->max_units = (int)max_units;
+  const int by_tmem = 512 / pl->shape.tmem_cols;
+  int by_smem = pl->shape.min_blocks;
+  if (have_dev && di.smem_per_sm > 0) by_smem = di.smem_per_sm / (int)(pl->shape.smem + 1024);
+  int cps = by_tmem < by_smem ? by_tmem : by_smem;
+  if (cps > pl->shape.min_blocks) cps = pl->shape.min_blocks;
+  if (cps < 1) cps = 1;
+  pl->ctas_per_sm = cps;
+  pl->smem_launch = pl->shape.smem;
+  if (have_dev && di.smem_per_sm > 0) {
+    // Request enough that a (cps+1)-th CTA cannot fit next to the others.
+    const unsigned pad = (unsigned)(di.smem_per_sm / (cps + 1)) + 1u;
+    if (pad > pl->smem_launch) pl->smem_launch = pad;
+  }
+  const int sms = have_dev ? di.sms : 152;
+  long long grid = (long long)sms * cps;
+  if (grid > max_units) grid = max_units;
+  if (grid < 1) grid = 1;
+  pl->grid = (int)grid;
+  return GQA_OK;
+}
+
+int encode_map(CUtensorMap* m, const void* base, int dtype, int d, int heads, int rows,
+               int box_heads, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return GQA_ERR_CUDA;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2u, (cuuint64_t)heads * d * 2u};
+  const cuuint32_t box[3] = {64u, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = fn(m,
+                        dtype == GQA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GQA_OK : GQA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int run(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+        const int32_t* prefix_lens, const int32_t* kv_indptr, int num_seqs, int total_q,
+        int total_kv, int max_seqlen_q, int Hq, int Hkv, int d, int dtype, float scale,
+        int window, const float* sinks, int smooth_softmax, void* out, float* lse, void* stream,
+        int32_t* unit_log) {
+  if (num_seqs < 0 || total_q < 0 || total_kv < 0 || max_seqlen_q < 0) return GQA_ERR_INVALID;
+  if (Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return GQA_ERR_INVALID;
+  if (dtype != GQA_F16 && dtype != GQA_BF16) return GQA_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return GQA_ERR_INVALID;
+  if (sinks != nullptr && smooth_softmax != 0) return GQA_ERR_INVALID;
+  if (num_seqs == 0 || total_q == 0) return GQA_OK;  // no work, no launch
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr ||
+      cu_seqlens_q == nullptr || prefix_lens == nullptr || kv_indptr == nullptr)
+    return GQA_ERR_INVALID;
+  if (total_kv == 0) return GQA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return GQA_ERR_INVALID;
+  Plan pl;
+  int rc = make_plan(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, &pl);
+  if (rc != GQA_OK) return rc;
+  DeviceInfo di;
+  if (device_info(&di) != GQA_OK) return GQA_ERR_CUDA;
+
+  PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  rc = encode_map(&p.tmap_q, q, dtype, d, Hq, total_q, pl.G, pl.rows);
+  if (rc == GQA_OK) rc = encode_map(&p.tmap_k, k, dtype, d, Hkv, total_kv, 1, pl.shape.block_n);
+  if (rc == GQA_OK) rc = encode_map(&p.tmap_v, v, dtype, d, Hkv, total_kv, 1, pl.shape.block_n);
+  if (rc != GQA_OK) return rc;
+  p.cu_seqlens_q = cu_seqlens_q;
+  p.prefix_lens = prefix_lens;
+  p.kv_indptr = kv_indptr;
+  p.sinks = sinks;
+  p.out = out;
+  p.lse = lse;
+  p.unit_log = unit_log;
+  p.status = di.status;
+  p.num_seqs = num_seqs;
+  p.total_q = total_q;
+  p.total_kv = total_kv;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = pl.G;
+  p.rows = pl.rows;
+  p.window = window > 0 ? window : 0;
+  p.smooth = smooth_softmax != 0 ? 1 : 0;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.timeout_ns = 4000000000ull;
+  if (const char* t = std::getenv("GQA_PREFILL_TIMEOUT_MS")) {
+    const long long ms = std::atoll(t);
+    if (ms > 0) p.timeout_ns = (unsigned long long)ms * 1000000ull;
+  }
+  const bool win = p.window > 0;
+  const bool bf16 = dtype == GQA_BF16;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (d == 64)
+    e = launch_d64(p, pl.shape.block_n, win, bf16, pl.grid, pl.smem_launch, st);
+  else if (d == 128)
+    e = launch_d128(p, pl.shape.block_n, win, bf16, pl.grid, pl.smem_launch, st);
+  else
+    e = launch_d256(p, pl.shape.block_n, win, bf16, pl.grid, pl.smem_launch, st);
+  if (env_flag("GQA_PREFILL_DEBUG"))
+    std::fprintf(stderr,
+                 "[gqa_prefill] B=%d total_q=%d total_kv=%d Hq=%d Hkv=%d d=%d %s window=%d "
+                 "sink=%s block_n=%d stages=%d grid=%d (%d/SM) max_units=%d -> %s\n",
+                 num_seqs, total_q, total_kv, Hq, Hkv, d, bf16 ? "bf16" : "f16", p.window,
+                 sinks ? "head" : (p.smooth ? "smooth" : "none"), pl.shape.block_n,
+                 pl.shape.kv_stages, pl.grid, pl.ctas_per_sm, pl.max_units,
+                 e == cudaSuccess ? "launched" : cudaGetErrorString(e));
+  return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+}  // namespace
+
+bool kernel_shape(int d, int block_n, KernelShape* out) {
+  KernelShape s;
+  s.block_n = block_n;
+  if (d == 64 && block_n == 128) { s.kv_stages = 2; s.min_blocks = 2; }
+  else if (d == 64 && block_n == 64) { s.kv_stages = 3; s.min_blocks = 2; }
+  else if (d == 128 && block_n == 64) { s.kv_stages = 2; s.min_blocks = 2; }
+  else if (d == 128 && block_n == 128) { s.kv_stages = 2; s.min_blocks = 1; }
+  else if (d == 256 && block_n == 64) { s.kv_stages = 2; s.min_blocks = 1; }
+  else return false;
+  s.smem = smem_bytes_for(d, block_n, s.kv_stages);
+  s.tmem_cols = tmem_cols_for(d, block_n);
+  *out = s;
+  return true;
+}
+
+}  // namespace gqa
+
+extern "C" {
+
+int gqa_flash_prefill(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                      const int32_t* prefix_lens, const int32_t* kv_indptr, int num_seqs,
+                      int total_q, int total_kv, int max_seqlen_q, int Hq, int Hkv, int d,
+                      int dtype, float scale, int window, const float* sinks, int smooth_softmax,
+                      void* out, float* lse, void* stream) {
+  return gqa::run(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs, total_q, total_kv,
+                  max_seqlen_q, Hq, Hkv, d, dtype, scale, window, sinks, smooth_softmax, out, lse,
+                  stream, nullptr);
+}
+
+int gqa_flash_prefill_debug(const void* q, const void* k, const void* v,
+                            const int32_t* cu_seqlens_q, const int32_t* prefix_lens,
+                            const int32_t* kv_indptr, int num_seqs, int total_q, int total_kv,
+                            int max_seqlen_q, int Hq, int Hkv, int d, int dtype, float scale,
+                            int window, const float* sinks, int smooth_softmax, void* out,
+                            float* lse, void* stream, int32_t* unit_log) {
+  if (unit_log == nullptr) return GQA_ERR_INVALID;
+  return gqa::run(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs, total_q, total_kv,
+                  max_seqlen_q, Hq, Hkv, d, dtype, scale, window, sinks, smooth_softmax, out, lse,
+                  stream, unit_log);
+}
+
+int gqa_prefill_plan(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, int d,
+                     int dtype, int window, gqa_prefill_plan_t* plan) {
+  if (plan == nullptr) return GQA_ERR_INVALID;
+  gqa::Plan pl;
+  const int rc =
+      gqa::make_plan(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, &pl);
+  if (rc != GQA_OK) return rc;
+  plan->rows_per_unit = pl.rows;
+  plan->block_n = pl.shape.block_n;
+  plan->kv_stages = pl.shape.kv_stages;
+  plan->ctas_per_sm = pl.ctas_per_sm;
+  plan->grid = pl.grid;
+  plan->max_units = pl.max_units;
+  return GQA_OK;
+}
+
+int gqa_prefill_force_block_n(int block_n) {
+  if (block_n != 0 && block_n != 64 && block_n != 128) return GQA_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(gqa::g_mu);
+  gqa::g_forced_block_n = block_n;
+  return GQA_OK;
+}
+
+int gqa_prefill_get_device_status(int* status) {
+  if (status == nullptr) return GQA_ERR_INVALID;
+  if (cudaDeviceSynchronize() != cudaSuccess) return GQA_ERR_CUDA;
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, gqa::g_device_status, sizeof(v)) != cudaSuccess) return GQA_ERR_CUDA;
+  if (cudaMemcpyToSymbol(gqa::g_device_status, &zero, sizeof(zero)) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  *status = (int)v;
+  return GQA_OK;
+}
+
+const char* gqa_prefill_status_string(int code) {
+  switch (code) {
+    case GQA_OK: return "ok";
+    case GQA_ERR_INVALID: return "invalid argument";
+    case GQA_ERR_UNSUPPORTED: return "unsupported shape (declined)";
+    case GQA_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+const char* gqa_prefill_version(void) { return "0.1.0"; }
+
+}  // extern "C"

@@ -1,0 +1,537 @@
+// prefill_kernel.cuh -- persistent, warp-specialised fused GQA flash-attention
+// prefill for sm_103a: TMA-fed K/V ring shared by the G query heads of a KV
+// head, tcgen05 MMAs into tensor memory for S = Q K^T and O += P V, online
+// exp2 softmax with the mask applied only on edge tiles, and the sink folded
+// into the denominator in the epilogue.
+//
+// Operation: hip-ep PR #622 "perf(gqa): support sliding windows in the fused
+// flash prefill kernel" (sink fold, window bound, start-tile clamp, NaN guard)
+// and SGLang PR #34468 "gfx950 SWA prefix trim" (one floored KV loop over
+// prefix and extend).  The AMD kernels on those pages are prior art only; the
+// structure here is GB300-specific.
+//
+// CTA = 6 warps.  Warps 0-3: softmax + epilogue, thread r owns row r of the
+// 128-row tile (tensor-memory lane r).  Warp 4: TMA producer.  Warp 5: tensor
+// memory allocation and the single-thread MMA issuer.
+//
+// Row packing: row r of a unit's tile is query head g*G + (r % G) at query
+// position q0 + r / G, which is the [token][head] order of q in memory, so
+// one 3-D TMA box (d-chunk, G heads, 128/G tokens) fills the tile and every
+// K/V tile is loaded once for all G heads of the group.
+#pragma once
+#include <cuda.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "tile_math.cuh"
+
+namespace gqa {
+
+constexpr int kMaxSeqs = 1024;       // sequences per call (smem tile table)
+constexpr int kThreads = 192;        // 6 warps
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+// Lazy rescale: the running max used as the exponent reference is only moved
+// when a row's max grows by more than this many powers of two; probabilities
+// are then bounded by 2^8, and the final division by the same-referenced
+// denominator makes the result exact regardless of the reference.
+constexpr float kRescaleThreshold = 8.0f;
+
+struct PrefillParams {
+  CUtensorMap tmap_q;  // [total_q, Hq, d]  box (64, G, 128/G), 128B swizzle
+  CUtensorMap tmap_k;  // [total_kv, Hkv, d] box (64, 1, BN)
+  CUtensorMap tmap_v;
+  const int32_t* cu_seqlens_q;
+  const int32_t* prefix_lens;
+  const int32_t* kv_indptr;
+  const float* sinks;
+  void* out;
+  float* lse;
+  int32_t* unit_log;
+  unsigned int* status;
+  int num_seqs, total_q, total_kv;
+  int Hq, Hkv, G, rows;  // rows = query positions per unit = 128 / G
+  int window;            // <= 0: none
+  int smooth;
+  float scale_log2;      // scale * log2(e)
+  unsigned long long timeout_ns;
+};
+
+__host__ __device__ constexpr int tmem_cols_for(int D, int BN) {
+  // S (BN fp32 columns) + P (BN 16-bit values = BN/2 columns) + O (D columns)
+  return (BN + BN / 2 + D) <= 32 ? 32
+         : (BN + BN / 2 + D) <= 64 ? 64
+         : (BN + BN / 2 + D) <= 128 ? 128
+         : (BN + BN / 2 + D) <= 256 ? 256
+                                    : 512;
+}
+
+__host__ __device__ constexpr uint32_t smem_bytes_for(int D, int BN, int NS) {
+  return 1024u                                  // alignment slack
+         + 128u * D * 2u                        // Q tile
+         + 2u * NS * BN * D * 2u                // K and V rings
+         + 64u * 8u                             // mbarriers
+         + 16u                                  // misc words
+         + 4u * (kMaxSeqs + 1) + 4u * kThreads; // tile table + scan scratch
+}
+
+// Barrier indices
+template <int NS>
+struct Bar {
+  static constexpr int kQFull = 0, kQEmpty = 1;
+  static constexpr int kKFull = 2, kKEmpty = 2 + NS, kVFull = 2 + 2 * NS, kVEmpty = 2 + 3 * NS;
+  static constexpr int kSFull = 2 + 4 * NS, kSFree = kSFull + 1, kPFull = kSFull + 2;
+  static constexpr int kODone = kSFull + 3, kOFree = kSFull + 4, kDrain = kSFull + 5;
+  static constexpr int kCount = kSFull + 6;
+};
+
+struct Unit {
+  int b, g, q0, q_last, P, E, kv_base, q_row0, kv_lo, n_tiles;
+};
+
+// Unit u -> (sequence, KV head, query tile).  Units are numbered with the KV
+// head fastest and, inside a sequence, the last (costliest under causality)
+// query tile first.
+__device__ __forceinline__ Unit decode_unit(const PrefillParams& p, const int32_t* tile_start,
+                                            int u, int BN) {
+  Unit U;
+  U.g = u % p.Hkv;
+  const int tau = u / p.Hkv;
+  int lo = 0, hi = p.num_seqs;  // find b with tile_start[b] <= tau < tile_start[b+1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tile_start[mid] <= tau) lo = mid; else hi = mid;
+  }
+  U.b = lo;
+  const int t = tau - tile_start[lo];
+  const int tiles_b = tile_start[lo + 1] - tile_start[lo];
+  U.q0 = (tiles_b - 1 - t) * p.rows;
+  U.P = __ldg(p.prefix_lens + U.b);
+  const int cu0 = __ldg(p.cu_seqlens_q + U.b);
+  U.E = __ldg(p.cu_seqlens_q + U.b + 1) - cu0;
+  U.q_last = min(U.q0 + p.rows, U.E) - 1;
+  U.q_row0 = cu0 + U.q0;
+  U.kv_base = __ldg(p.kv_indptr + U.b);
+  const KvRange r = kv_range(U.P, U.q0, U.q_last, p.window, BN);
+  U.kv_lo = r.kv_lo;
+  U.n_tiles = r.n_tiles;
+  return U;
+}
+
+// k-th unit of this CTA: round k of a snake (boustrophedon) deal over the
+// grid, so that with units ordered by decreasing cost every CTA alternates
+// between the expensive and the cheap end of each round.
+__device__ __forceinline__ int unit_of(int k) {
+  const int g = gridDim.x, c = blockIdx.x;
+  return k * g + ((k & 1) ? (g - 1 - c) : c);
+}
+
+// Bounded mbarrier wait.  Returns false (and raises the abort flag and the
+// device status) when the phase does not complete within the time limit or
+// when another role of this CTA has aborted.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile uint32_t* abort_flag,
+                                             unsigned int* status,
+                                             unsigned long long timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > timeout_ns) {
+        *abort_flag = 1u;
+        atomicOr(status, 1u);  // GQA_DEV_TIMEOUT
+        return false;
+      }
+    }
+  }
+}
+
+}  // namespace gqa
+
+namespace gqa {
+
+// Bounded wait used while draining at exit: ignores the abort flag, because
+// its purpose is to let copies and MMAs already in flight land before the CTA
+// releases its shared and tensor memory.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity,
+                                           unsigned long long timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((n & 255u) == 0 && globaltimer_ns() - t0 > timeout_ns) return;
+  }
+}
+
+template <int D, int BN, int NS, bool WIN, bool BF16, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
+    prefill_kernel(const __grid_constant__ PrefillParams p) {
+  static_assert(D == 64 || D == 128 || D == 256, "head dim");
+  static_assert(BN == 64 || BN == 128, "key tile");
+  constexpr int NCH = D / 64;  // 128-byte swizzle chunks along d
+  constexpr uint32_t kQBytes = 128u * D * 2u;
+  constexpr uint32_t kKVBytes = (uint32_t)BN * D * 2u;
+  constexpr uint32_t kQChunk = 128u * 128u;
+  constexpr uint32_t kKVChunk = (uint32_t)BN * 128u;
+  constexpr uint32_t kTmemCols = (uint32_t)tmem_cols_for(D, BN);
+  constexpr uint32_t kColS = 0, kColP = BN, kColO = BN + BN / 2;
+  constexpr uint32_t kIdescS = idesc_f16(BF16, 128, BN, false);  // Q, K both K-major
+  constexpr uint32_t kIdescO = idesc_f16(BF16, 128, D, true);    // V is MN-major
+  using B = Bar<NS>;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sQ = smem_u32(smem);
+  const uint32_t sK = sQ + kQBytes;
+  const uint32_t sV = sK + NS * kKVBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQBytes + 2 * NS * kKVBytes);
+  const uint32_t sBar = smem_u32(bars);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 64);  // [0] tmem base, [1] abort, [2] bad
+  int32_t* tile_start = reinterpret_cast<int32_t*>(misc + 4);
+  int32_t* scan = tile_start + (kMaxSeqs + 1);
+  volatile uint32_t* abort_flag = misc + 1;
+  const unsigned long long tmo = p.timeout_ns;
+  const int win = WIN ? p.window : 0;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---------------------------------------------------------------- set-up
+  if (tid == 0) {
+    for (int i = 0; i < B::kCount; ++i)
+      mbar_init(sBar + 8u * i, (i == B::kSFree || i == B::kPFull) ? 128u : 1u);
+    misc[1] = 0u;
+    misc[2] = 0u;
+    fence_barrier_init();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&p.tmap_q);
+    tma_prefetch_desc(&p.tmap_k);
+    tma_prefetch_desc(&p.tmap_v);
+  }
+  __syncthreads();
+
+  // Per-sequence query-tile counts, their exclusive scan, and the metadata
+  // checks (bad metadata: write nothing, raise GQA_DEV_BAD_METADATA).
+  const int nseq = p.num_seqs;
+  const int per = (nseq + kThreads - 1) / kThreads;
+  const int b_lo = min(tid * per, nseq), b_hi = min(b_lo + per, nseq);
+  int local = 0;
+  bool bad = (tid == 0) && (__ldg(p.cu_seqlens_q) != 0);
+  for (int b = b_lo; b < b_hi; ++b) {
+    const int c0 = __ldg(p.cu_seqlens_q + b), c1 = __ldg(p.cu_seqlens_q + b + 1);
+    const int P = __ldg(p.prefix_lens + b);
+    const int k0 = __ldg(p.kv_indptr + b), k1 = __ldg(p.kv_indptr + b + 1);
+    const int E = c1 - c0;
+    if (E < 0 || P < 0 || c0 < 0 || c1 > p.total_q || k0 < 0 || k1 > p.total_kv ||
+        (long long)k1 - k0 != (long long)P + E)
+      bad = true;
+    else
+      local += (E + p.rows - 1) / p.rows;
+  }
+  scan[tid] = local;
+  if (bad) misc[2] = 1u;
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int i = 0; i < kThreads; ++i) {
+      const int v = scan[i];
+      scan[i] = acc;
+      acc += v;
+    }
+    tile_start[nseq] = acc;
+  }
+  __syncthreads();
+  {
+    int acc = scan[tid];
+    for (int b = b_lo; b < b_hi; ++b) {
+      tile_start[b] = acc;
+      const int E = __ldg(p.cu_seqlens_q + b + 1) - __ldg(p.cu_seqlens_q + b);
+      acc += E > 0 ? (E + p.rows - 1) / p.rows : 0;
+    }
+  }
+  __syncthreads();
+  if (misc[2] != 0u) {
+    if (tid == 0) atomicOr(p.status, 2u);  // GQA_DEV_BAD_METADATA
+    return;
+  }
+  const int n_units = tile_start[nseq] * p.Hkv;
+  if (blockIdx.x >= n_units) return;  // nothing for this CTA (before any TMEM use)
+
+  if (warp == 5) {
+    tmem_alloc(smem_u32(misc), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  // ---------------------------------------------------------------- producer
+  if (warp == 4) {
+    if (lane == 0) {
+      uint32_t it = 0, uc = 0, nk[NS], nv[NS];
+      for (int s = 0; s < NS; ++s) nk[s] = nv[s] = 0u;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int u = unit_of(k);
+        if (u >= n_units) break;
+        const Unit U = decode_unit(p, tile_start, u, BN);
+        if (!(ok = wait_bounded(sBar + 8u * B::kQEmpty, (uc & 1u) ^ 1u, abort_flag, p.status, tmo)))
+          break;
+        mbar_arrive_expect_tx(sBar + 8u * B::kQFull, kQBytes);
+        for (int c = 0; c < NCH; ++c)
+          tma_load_3d(sQ + c * kQChunk, &p.tmap_q, sBar + 8u * B::kQFull, c * 64, U.g * p.G,
+                      U.q_row0);
+        ++uc;
+        for (int j = 0; j < U.n_tiles; ++j, ++it) {
+          const uint32_t s = it % NS, ph = (it / NS) & 1u;
+          const int row = U.kv_base + U.kv_lo + j * BN;
+          if (!(ok = wait_bounded(sBar + 8u * (B::kKEmpty + s), ph ^ 1u, abort_flag, p.status, tmo)))
+            break;
+          mbar_arrive_expect_tx(sBar + 8u * (B::kKFull + s), kKVBytes);
+          for (int c = 0; c < NCH; ++c)
+            tma_load_3d(sK + s * kKVBytes + c * kKVChunk, &p.tmap_k, sBar + 8u * (B::kKFull + s),
+                        c * 64, U.g, row);
+          ++nk[s];
+          if (!(ok = wait_bounded(sBar + 8u * (B::kVEmpty + s), ph ^ 1u, abort_flag, p.status, tmo)))
+            break;
+          mbar_arrive_expect_tx(sBar + 8u * (B::kVFull + s), kKVBytes);
+          for (int c = 0; c < NCH; ++c)
+            tma_load_3d(sV + s * kKVBytes + c * kKVChunk, &p.tmap_v, sBar + 8u * (B::kVFull + s),
+                        c * 64, U.g, row);
+          ++nv[s];
+        }
+      }
+      // Let every copy issued land before the CTA can exit.
+      if (uc > 0) wait_drain(sBar + 8u * B::kQFull, (uc - 1u) & 1u, tmo);
+      for (int s = 0; s < NS; ++s) {
+        if (nk[s] > 0) wait_drain(sBar + 8u * (B::kKFull + s), (nk[s] - 1u) & 1u, tmo);
+        if (nv[s] > 0) wait_drain(sBar + 8u * (B::kVFull + s), (nv[s] - 1u) & 1u, tmo);
+      }
+    }
+    __syncwarp();
+  }
+
+  // ---------------------------------------------------------------- MMA issuer
+  if (warp == 5) {
+    if (lane == 0) {
+      // Q and K: K-major, 128-byte swizzle; the 16-wide k-step advances the
+      // start address by 32 bytes inside a 128-byte swizzle row, the 64-wide
+      // d-chunk by one chunk.  Stride between 8-row groups: 1024 bytes.
+      auto qdesc = [&](int kk) {
+        return smem_desc_sw128(sQ + (kk >> 2) * kQChunk + (kk & 3) * 32, 16, 1024);
+      };
+      auto kdesc = [&](uint32_t s, int kk) {
+        return smem_desc_sw128(sK + s * kKVBytes + (kk >> 2) * kKVChunk + (kk & 3) * 32, 16, 1024);
+      };
+      // V: MN-major (d contiguous), 128-byte swizzle; a 16-key step is two
+      // 8-key groups = 2048 bytes; d-chunks of 64 are kKVChunk apart.
+      auto vdesc = [&](uint32_t s, int kk) {
+        return smem_desc_sw128(sV + s * kKVBytes + kk * 2048, kKVChunk, 1024);
+      };
+      auto issue_pv = [&](uint32_t itp, bool first) -> bool {
+        const uint32_t sp = itp % NS, php = (itp / NS) & 1u;
+        if (!wait_bounded(sBar + 8u * (B::kVFull + sp), php, abort_flag, p.status, tmo)) return false;
+        if (!wait_bounded(sBar + 8u * B::kPFull, itp & 1u, abort_flag, p.status, tmo)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tmem + kColO, tmem + kColP + kk * 8, vdesc(sp, kk), kIdescO,
+                 (first && kk == 0) ? 0u : 1u);
+        mma_commit(sBar + 8u * B::kODone);
+        mma_commit(sBar + 8u * (B::kVEmpty + sp));
+        return true;
+      };
+      uint32_t it = 0, uc = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int u = unit_of(k);
+        if (u >= n_units) break;
+        const Unit U = decode_unit(p, tile_start, u, BN);
+        if (!(ok = wait_bounded(sBar + 8u * B::kQFull, uc & 1u, abort_flag, p.status, tmo))) break;
+        for (int j = 0; j < U.n_tiles; ++j) {
+          const uint32_t cur = it + j;
+          const uint32_t s = cur % NS, ph = (cur / NS) & 1u;
+          if (!(ok = wait_bounded(sBar + 8u * (B::kKFull + s), ph, abort_flag, p.status, tmo))) break;
+          if (cur > 0 &&
+              !(ok = wait_bounded(sBar + 8u * B::kSFree, (cur - 1u) & 1u, abort_flag, p.status, tmo)))
+            break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + kColS, qdesc(kk), kdesc(s, kk), kIdescS, kk > 0 ? 1u : 0u);
+          mma_commit(sBar + 8u * B::kSFull);
+          mma_commit(sBar + 8u * (B::kKEmpty + s));
+          if (j == U.n_tiles - 1) mma_commit(sBar + 8u * B::kQEmpty);
+          // PV of the previous tile goes after this tile's QK^T, so the
+          // tensor core works on S(j) while the softmax warps work on S(j-1).
+          if (j > 0 && !(ok = issue_pv(cur - 1u, j == 1))) break;
+        }
+        if (ok) ok = issue_pv(it + U.n_tiles - 1u, U.n_tiles == 1);
+        it += U.n_tiles;
+        ++uc;
+      }
+      mma_commit(sBar + 8u * B::kDrain);  // completes when every MMA issued is done
+      wait_drain(sBar + 8u * B::kDrain, 0u, tmo);
+    }
+    __syncwarp();
+  }
+
+  // ---------------------------------------------------------------- softmax + epilogue
+  if (warp < 4) {
+    const int r = tid;  // tile row == tensor-memory lane
+    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+    const float sl2 = p.scale_log2;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int u = unit_of(k);
+      if (u >= n_units) break;
+      const Unit U = decode_unit(p, tile_start, u, BN);
+      const int pl = U.q0 + r / p.G;  // query position inside the sequence
+      const int h = U.g * p.G + r % p.G;
+      const int pos = U.P + pl;
+      float m = -INFINITY;  // exponent reference (log2 domain)
+      float l = 0.f;        // running denominator, relative to m
+      int n_masked = 0;
+      for (int j = 0; j < U.n_tiles; ++j, ++it) {
+        const int n0 = U.kv_lo + j * BN;
+        ok = __all_sync(0xffffffffu,
+                        wait_bounded(sBar + 8u * B::kSFull, it & 1u, abort_flag, p.status, tmo));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c)
+          tmem_ld32(t_lane + kColS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(sBar + 8u * B::kSFree);  // S is in registers: next QK^T may overwrite it
+
+        // Per-element mask, edge tiles only (the decision is uniform over the CTA).
+        if (tile_needs_mask(n0, BN, U.P, U.q0, U.q_last, win)) {
+          ++n_masked;
+          const int lo = pos - win + 1;
+#pragma unroll
+          for (int c = 0; c < BN; ++c) {
+            const int key = n0 + c;
+            if (key > pos || (WIN && key < lo)) sr[c] = __float_as_uint(-INFINITY);
+          }
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < BN; c += 2)
+          mx = max3(mx, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+        const float m_cand = mx * sl2;
+        const bool upd = m_cand > m + kRescaleThreshold;
+        const float m_new = upd ? m_cand : m;
+        const float alpha = upd ? ex2(m - m_new) : 1.f;
+        // NaN guard: a row that has seen no key keeps m = -inf; its scores
+        // are all -inf, and with a zero offset every probability is exactly 0.
+        const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
+        float sum0 = 0.f, sum1 = 0.f;
+        uint32_t pk[BN / 2];
+#pragma unroll
+        for (int c = 0; c < BN; c += 2) {
+          const float p0 = ex2(fmaf(__uint_as_float(sr[c]), sl2, neg_m));
+          const float p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), sl2, neg_m));
+          sum0 += p0;
+          sum1 += p1;
+          pk[c / 2] = pack2<BF16>(p0, p1);
+        }
+        l = l * alpha + (sum0 + sum1);
+        m = m_new;
+
+        // P and O are touched only once the previous PV has finished.
+        if (it > 0)
+          ok = __all_sync(0xffffffffu, wait_bounded(sBar + 8u * B::kODone, (it - 1u) & 1u,
+                                                     abort_flag, p.status, tmo));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < BN / 64; ++c)
+          tmem_st32(t_lane + kColP + c * 32, *reinterpret_cast<uint32_t(*)[32]>(pk + c * 32));
+        const bool corr = upd && j > 0;
+        if (__any_sync(0xffffffffu, corr)) {
+          const float a = corr ? alpha : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(t_lane + kColO + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+            tmem_st32(t_lane + kColO + c * 32, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(sBar + 8u * B::kPFull);
+      }
+      if (!ok) break;
+
+      // Epilogue: fold the sink into the denominator, normalise, store.
+      ok = __all_sync(0xffffffffu, wait_bounded(sBar + 8u * B::kODone, (it - 1u) & 1u, abort_flag,
+                                                 p.status, tmo));
+      if (!ok) break;
+      tc_fence_after();
+      const bool has_x = (p.sinks != nullptr) || (p.smooth != 0);
+      const float ms = (p.sinks != nullptr) ? __ldg(p.sinks + h) * kLog2e : 0.f;
+      float inv = 0.f, lse2 = -INFINITY;
+      if (m != -INFINITY) {
+        // Same value as l + exp2(ms - m) over the m-referenced sums, computed
+        // against max(m, ms) so that a large sink cannot overflow.
+        const float mf = has_x ? fmaxf(m, ms) : m;
+        const float a = ex2(m - mf);
+        float den = l * a + (has_x ? ex2(ms - mf) : 0.f);
+        den = fmaxf(den, 1e-30f);
+        inv = a / den;
+        lse2 = mf + log2f(den);
+      }
+      const bool valid = pl <= U.q_last;
+      const size_t orow = (size_t)(U.q_row0 + r / p.G) * p.Hq + h;
+      uint16_t* op = reinterpret_cast<uint16_t*>(p.out) + orow * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(t_lane + kColO + c * 32, o);
+        tmem_wait_ld();
+        if (valid) {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(op + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      if (valid && p.lse != nullptr) p.lse[orow] = lse2 * kLn2;
+      if (p.unit_log != nullptr && r == 0) {
+        int32_t* rec = p.unit_log + 8 * (size_t)u;
+        rec[0] = U.b;
+        rec[1] = U.g;
+        rec[2] = U.q0;
+        rec[3] = U.kv_lo;
+        rec[4] = U.n_tiles;
+        rec[5] = n_masked;
+        rec[6] = (int)blockIdx.x;
+        rec[7] = k;
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace gqa

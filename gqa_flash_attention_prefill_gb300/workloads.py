@@ -56,19 +56,24 @@ class Batch:
 
     @property
     def max_seqlen_q(self) -> int:
-        e = self.extend_lens
-        return max(e) if e else 0
+        if "max_seqlen_q" not in self.meta:  # host copy, kept across .to()
+            e = self.extend_lens
+            self.meta["max_seqlen_q"] = max(e) if e else 0
+        return self.meta["max_seqlen_q"]
 
     @property
     def extend_lens(self) -> List[int]:
-        cu = self.cu_seqlens_q.tolist()
-        return [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
+        if "extend_lens" not in self.meta:
+            cu = self.cu_seqlens_q.tolist()
+            self.meta["extend_lens"] = [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
+        return self.meta["extend_lens"]
 
     @property
     def dtype_name(self) -> str:
         return "bf16" if self.q.dtype == torch.bfloat16 else "f16"
 
     def to(self, device) -> "Batch":
+        self.max_seqlen_q  # cache host-side metadata before the move
         mv = lambda t: None if t is None else t.to(device)
         return Batch(mv(self.q), mv(self.k), mv(self.v), mv(self.cu_seqlens_q),
                      mv(self.prefix_lens), mv(self.kv_indptr), self.hq, self.hkv,

@@ -1,0 +1,174 @@
+/*
+ * gqa_prefill.h -- C ABI of libgqa_prefill.so: fused grouped-query
+ * flash-attention prefill for gpt-oss-style layers on sm_103a.
+ *
+ * The operation (what one call computes) follows two pages:
+ *   ROCm/hip-ep PR #622, "perf(gqa): support sliding windows in the fused
+ *   flash prefill kernel": the sink folded into the softmax denominator
+ *   (sink-fold commit), the smooth_softmax "+1" mode (sink-gate and
+ *   sink-harness commits), the per-row window bound and the KV-loop start
+ *   tile (window-in-v5 commit and the PR body "Why" / "A NaN the window
+ *   introduces"), and the decline-instead-of-miscompute rule (sink-fold
+ *   commit);
+ *   sgl-project/sglang PR #34468, "gfx950 SWA prefix trim": one KV loop over
+ *   [cached prefix | extend] with a BLOCK_N-aligned floor (commit 2), and the
+ *   window-bounded prefix layout (commit 1).
+ *
+ * Definition.  Sequence b has P_b = prefix_lens[b] cached keys followed by
+ * E_b = cu_seqlens_q[b+1] - cu_seqlens_q[b] new tokens.  Query row i of the
+ * sequence sits at position P_b + i and, for query head h, attends to key j
+ * of KV head h / (Hq/Hkv) iff j <= P_b + i and (window <= 0 or
+ * j >= P_b + i - window + 1): window counts the keys a row sees, itself
+ * included, so window = 1 is "itself only".  With s_j = scale * <q, k_j>
+ * over the kept keys and x the sink logit (sinks[h] in per-head mode, 0 in
+ * smooth_softmax mode, absent otherwise):
+ *     out = sum_j e^{s_j} v_j / (sum_j e^{s_j} + e^{x})
+ *     lse = log(sum_j e^{s_j} + e^{x})        (natural log)
+ * The sink is a natural-log logit and is NOT multiplied by scale.  A row
+ * with no kept key (impossible for real rows with consistent metadata)
+ * gets out = 0 and lse = -inf.
+ *
+ * Layouts (all row-major, dense, caller-owned device memory):
+ *   q, out  [total_q,  Hq,  d]   16-bit (dtype), 16-byte aligned base
+ *   k, v    [total_kv, Hkv, d]   same dtype; sequence b's keys are rows
+ *           kv_indptr[b] .. kv_indptr[b+1]-1, ordered [prefix | extend], so
+ *           kv_indptr[b+1] - kv_indptr[b] == P_b + E_b.  For a windowed
+ *           layer the caller may hand only the last min(prefix, window)
+ *           prefix rows (window-bounded layout): positions are relative to
+ *           the first supplied key, and the result is the same.
+ *   cu_seqlens_q  int32 [num_seqs+1], cu[0] = 0, non-decreasing, cu[B] <= total_q
+ *   prefix_lens   int32 [num_seqs]
+ *   kv_indptr     int32 [num_seqs+1], kv_indptr[B] <= total_kv
+ *   sinks         fp32 [Hq] or NULL
+ *   lse           fp32 [total_q, Hq] or NULL
+ * Every row of k and v in [0, total_kv) must hold finite values: the kernel
+ * reads whole key tiles and relies on masked probabilities being exact zeros.
+ *
+ * Ownership and asynchrony: the library allocates nothing per call and keeps
+ * only a process-wide launch-configuration cache.  A call validates its host
+ * arguments, enqueues one kernel on `stream` (a cudaStream_t; NULL = legacy
+ * default stream) and returns without synchronising; it never copies device
+ * data to the host.  Rows of out/lse that belong to no sequence are not
+ * written.
+ *
+ * Errors: invalid host arguments return GQA_ERR_INVALID before any launch;
+ * shapes the kernels do not implement return GQA_ERR_UNSUPPORTED (the call
+ * declines rather than computing something else); a failed launch returns
+ * GQA_ERR_CUDA.  Device metadata is checked by the kernel itself: if
+ * cu_seqlens_q / prefix_lens / kv_indptr are inconsistent the kernel writes
+ * nothing and raises GQA_DEV_BAD_METADATA in the device status word, read
+ * with gqa_prefill_get_device_status().  Every wait inside the kernel is
+ * bounded; a wait that runs out raises GQA_DEV_TIMEOUT instead of hanging.
+ */
+#ifndef GQA_PREFILL_H
+#define GQA_PREFILL_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of q, k, v and out. */
+enum { GQA_F16 = 0, GQA_BF16 = 1 };
+
+/* Host-side return codes. */
+enum {
+    GQA_OK = 0,
+    GQA_ERR_INVALID = -1,
+    GQA_ERR_UNSUPPORTED = -2,
+    GQA_ERR_CUDA = -3
+};
+
+/* Device status word bits (gqa_prefill_get_device_status). */
+enum {
+    GQA_DEV_TIMEOUT = 1,       /* a bounded wait inside a kernel ran out */
+    GQA_DEV_BAD_METADATA = 2   /* cu_seqlens_q / prefix_lens / kv_indptr inconsistent */
+};
+
+/*
+ * gqa_flash_prefill -- the fused prefill (see the definition above).
+ *   num_seqs     B >= 0
+ *   total_q      rows of q/out (>= cu_seqlens_q[B]); 0 means no work
+ *   total_kv     rows of k/v (>= kv_indptr[B])
+ *   max_seqlen_q optional host hint, max_b E_b (0 = unknown); only used to
+ *                pick a launch configuration, never to bound work
+ *   Hq, Hkv      query / KV heads, Hq % Hkv == 0; G = Hq/Hkv must divide 128
+ *   d            head dim: 64, 128 or 256
+ *   dtype        GQA_F16 or GQA_BF16
+ *   scale        multiplier of q.k (> 0, finite), usually 1/sqrt(d)
+ *   window       <= 0: causal only; else keys (pos - window, pos]
+ *   sinks        per-head logits or NULL; smooth_softmax must then be 0
+ *   smooth_softmax nonzero: +1 in the denominator (sinks must be NULL)
+ * Returns GQA_OK or a negative GQA_ERR_* code.
+ */
+int gqa_flash_prefill(const void* q, const void* k, const void* v,
+                      const int32_t* cu_seqlens_q, const int32_t* prefix_lens,
+                      const int32_t* kv_indptr, int num_seqs, int total_q,
+                      int total_kv, int max_seqlen_q, int Hq, int Hkv, int d,
+                      int dtype, float scale, int window, const float* sinks,
+                      int smooth_softmax, void* out, float* lse, void* stream);
+
+/*
+ * Launch plan of a call with these shapes (host only, no device access).
+ * A work unit is (sequence, KV head, query tile): the kernel's 128-row MMA
+ * tile packs the G query heads of one KV head over rows_per_unit query
+ * positions (rows_per_unit * G = 128), and walks keys in tiles of block_n.
+ */
+typedef struct {
+    int rows_per_unit;  /* query positions per unit (128 / G) */
+    int block_n;        /* keys per KV tile */
+    int kv_stages;      /* K/V shared-memory ring depth */
+    int ctas_per_sm;    /* resident CTAs per SM the launch assumes */
+    int grid;           /* CTAs launched (persistent) */
+    int max_units;      /* upper bound on units: Hkv * (ceil(total_q/rows) + B) */
+} gqa_prefill_plan_t;
+
+int gqa_prefill_plan(int num_seqs, int total_q, int max_seqlen_q, int Hq,
+                     int Hkv, int d, int dtype, int window,
+                     gqa_prefill_plan_t* plan);
+
+/*
+ * gqa_flash_prefill_debug -- same computation as gqa_flash_prefill, and each
+ * work unit also writes one record of 8 int32 into unit_log (device memory,
+ * capacity max_units records from gqa_prefill_plan; caller pre-fills it,
+ * e.g. with -1) at the unit's index:
+ *   b, g, q0, kv_lo, n_tiles, n_masked, cta, order
+ * kv_lo / n_tiles are the key tiles the unit walked (kv_lo relative to the
+ * sequence's first key), n_masked how many of them needed the per-element
+ * mask, cta the CTA that ran it and order its position in that CTA's list.
+ */
+int gqa_flash_prefill_debug(const void* q, const void* k, const void* v,
+                            const int32_t* cu_seqlens_q,
+                            const int32_t* prefix_lens, const int32_t* kv_indptr,
+                            int num_seqs, int total_q, int total_kv,
+                            int max_seqlen_q, int Hq, int Hkv, int d, int dtype,
+                            float scale, int window, const float* sinks,
+                            int smooth_softmax, void* out, float* lse,
+                            void* stream, int32_t* unit_log);
+
+/*
+ * Force the KV tile size for later calls in this process (0 restores the
+ * configuration cache's choice).  Valid values: 64 or 128 (d = 256 allows 64
+ * only).  Returns GQA_OK or GQA_ERR_INVALID.  Meant for tests and tuning.
+ */
+int gqa_prefill_force_block_n(int block_n);
+
+/*
+ * Read and clear the device status word of the current device (bits
+ * GQA_DEV_*).  Synchronises the device first.  Returns GQA_OK or
+ * GQA_ERR_CUDA; *status receives the bits.
+ */
+int gqa_prefill_get_device_status(int* status);
+
+/* Static text for a GQA_* return code. */
+const char* gqa_prefill_status_string(int code);
+
+/* Library version, e.g. "0.1.0". */
+const char* gqa_prefill_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_PREFILL_H */

@@ -1,0 +1,113 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+function include/gqa_prefill.h declares, and rejects invalid host arguments
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gqa_prefill.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gqa_flash_attention_prefill_gb300 import build
+    path = build.build()
+    import gqa_flash_attention_prefill_gb300 as pkg
+    return pkg.load(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gqa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    import gqa_flash_attention_prefill_gb300 as pkg
+    assert names == sorted(pkg.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.gqa_prefill_version().decode().count(".") == 2
+    for code in (0, -1, -2, -3):
+        assert lib.gqa_prefill_status_string(code)
+
+
+FAKE = 1 << 20  # a 16-byte-aligned non-null address; never dereferenced
+
+
+def _call(lib, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, cu=FAKE, pre=FAKE, kvi=FAKE, B=1, total_q=16,
+             total_kv=16, max_q=16, hq=8, hkv=2, d=64, dtype=1, scale=0.125, window=0,
+             sinks=None, smooth=0, out=FAKE, lse=None, stream=None)
+    a.update(over)
+    return lib.gqa_flash_prefill(a["q"], a["k"], a["v"], a["cu"], a["pre"], a["kvi"], a["B"],
+                                 a["total_q"], a["total_kv"], a["max_q"], a["hq"], a["hkv"],
+                                 a["d"], a["dtype"], a["scale"], a["window"], a["sinks"],
+                                 a["smooth"], a["out"], a["lse"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(hq=6, hkv=4), -1),            # Hq % Hkv != 0
+    (dict(hkv=0), -1),
+    (dict(d=0), -1),
+    (dict(dtype=7), -1),
+    (dict(scale=0.0), -1),
+    (dict(scale=-1.0), -1),
+    (dict(scale=float("inf")), -1),
+    (dict(scale=float("nan")), -1),
+    (dict(sinks=FAKE, smooth=1), -1),   # the sink modes are exclusive
+    (dict(B=-1), -1),
+    (dict(total_q=-5), -1),
+    (dict(q=None), -1),
+    (dict(out=None), -1),
+    (dict(cu=None), -1),
+    (dict(kvi=None), -1),
+    (dict(q=FAKE + 8), -1),             # misaligned base
+    (dict(out=FAKE + 2), -1),
+    (dict(total_kv=0), -1),
+    (dict(d=96), -2),                   # declined: head dim not implemented
+    (dict(hq=24, hkv=1), -2),           # declined: G does not divide 128
+    (dict(B=4096), -2),                 # declined: more sequences than the tile table
+])
+def test_invalid_arguments_are_rejected_before_launch(lib, over, code):
+    assert _call(lib, **over) == code
+
+
+def test_empty_work_is_ok_without_launch(lib):
+    assert _call(lib, B=0) == 0
+    assert _call(lib, total_q=0) == 0
+    assert _call(lib, B=0, q=None, k=None, v=None, out=None) == 0
+
+
+def test_plan_is_host_only(lib):
+    import gqa_flash_attention_prefill_gb300 as pkg
+    p = pkg.plan(1, 4096, 4096, 64, 8, 64, "bf16", 0)
+    assert p["rows_per_unit"] == 16 and p["block_n"] in (64, 128)
+    assert p["max_units"] == 8 * (4096 // 16 + 1)
+    assert p["grid"] >= 1
+    p = pkg.plan(1, 256, 256, 4, 1, 64, "f16", 32)
+    assert p["rows_per_unit"] == 32
+    with pytest.raises(pkg.GQAError):
+        pkg.plan(1, 10, 10, 8, 2, 80, "bf16", 0)
+
+
+def test_force_block_n_validates(lib):
+    assert lib.gqa_prefill_force_block_n(96) == -1
+    assert lib.gqa_prefill_force_block_n(64) == 0
+    assert lib.gqa_prefill_force_block_n(0) == 0
+
+
+def test_binding_refuses_to_run_without_library(tmp_path):
+    import gqa_flash_attention_prefill_gb300 as pkg
+    with pytest.raises(RuntimeError, match="missing"):
+        pkg.load(str(tmp_path / "nope.so"))

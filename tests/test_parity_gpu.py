@@ -1,0 +1,271 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.  Full outputs on sizes the oracle finishes quickly (several
+tiles plus ragged tails); sampled rows at the full workload sizes, in the same
+launch configuration the benchmark uses."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gqa_flash_attention_prefill_gb300 import workloads as W
+from parity_util import (compare, run_gpu, run_oracle, sample_rows, sub_batch)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    import __graft_entry__
+    __graft_entry__.build()
+    import gqa_flash_attention_prefill_gb300 as pkg
+    pkg.load()
+    pkg.force_block_n(0)
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return pkg
+
+
+def _check_full(pkg, batch, label=None):
+    out, lse = run_gpu(pkg, batch)
+    ref, ref_lse = run_oracle(batch)
+    return compare(out, lse, ref, ref_lse, label=label or batch.name)
+
+
+def _check_sampled(pkg, batch, rows, label=None):
+    out, lse = run_gpu(pkg, batch)
+    ref, ref_lse = run_oracle(batch, rows=rows)
+    return compare(out, lse, ref, ref_lse, rows=rows, label=label or batch.name)
+
+
+# ------------------------------------------------------------- small, full output
+
+def test_tiny_config(pkg):
+    _check_full(pkg, W.tiny(seed=0))
+
+
+SMALL_WINDOWS = [0, 1, 15, 64, 100, 129]
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("window", SMALL_WINDOWS)
+@pytest.mark.parametrize("sink_mode", ["none", "head", "smooth"])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_small_ragged_grid(pkg, d, window, sink_mode, dtype):
+    b = W.make_batch([0, 37, 200, 5], [1, 150, 77, 33], 16, 2, d, dtype,
+                     window=window, sink_mode=sink_mode,
+                     seed=1000 + d + window * 7 + len(sink_mode))
+    _check_full(pkg, b)
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (8, 2), (64, 8), (32, 4), (128, 1)])
+def test_group_sizes(pkg, hq, hkv):
+    b = W.make_batch([3, 130], [70, 129], hq, hkv, 64, "bf16", window=33,
+                     sink_mode="head", seed=hq * 31 + hkv)
+    _check_full(pkg, b)
+
+
+@pytest.mark.parametrize("d,block_n", [(64, 64), (64, 128), (128, 64), (128, 128), (256, 64)])
+@pytest.mark.parametrize("window", [0, 100])
+def test_block_n_variants(pkg, d, block_n, window):
+    pkg.force_block_n(block_n)
+    try:
+        b = W.make_batch([0, 190], [300, 257], 16, 2, d, "bf16", window=window,
+                         sink_mode="head", seed=d + block_n + window)
+        _check_full(pkg, b, label=f"d{d}/bn{block_n}/w{window}")
+    finally:
+        pkg.force_block_n(0)
+
+
+def test_layer_pair_small_full_output(pkg):
+    for b in W.layer_pair(seq=640, seed=1):
+        _check_full(pkg, b)
+
+
+def test_chunked_prefix_small_both_layouts(pkg):
+    full = W.chunked_prefix(num_seqs=2, prefix=300, extend=200, window=128, seed=2)
+    bounded = W.window_bounded(full, 128)
+    a_out, a_lse = run_gpu(pkg, full)
+    b_out, b_lse = run_gpu(pkg, bounded)
+    ref, ref_lse = run_oracle(full)
+    compare(a_out, a_lse, ref, ref_lse, label="full-prefix layout")
+    compare(b_out, b_lse, ref, ref_lse, label="window-bounded layout")
+
+
+def test_chunked_equals_one_shot(pkg):
+    one = W.make_batch([0], [700], 64, 8, 64, "bf16", window=0, sink_mode="head", seed=5)
+    ref_out, ref_lse = run_gpu(pkg, one)
+    for a, c in [(0, 130), (130, 131), (131, 512), (512, 700)]:
+        chunk = W.Batch(one.q[a:c], one.k[:c], one.v[:c],
+                        torch.tensor([0, c - a], dtype=torch.int32),
+                        torch.tensor([a], dtype=torch.int32),
+                        torch.tensor([0, c], dtype=torch.int32), one.hq, one.hkv,
+                        one.d, one.window, one.sinks, one.smooth, one.scale)
+        out, lse = run_gpu(pkg, chunk)
+        compare(out, lse, ref_out[a:c].double().numpy(), ref_lse[a:c].double().numpy(),
+                label=f"chunk {a}:{c}")
+
+
+def test_padding_rows_untouched_and_empty_sequences(pkg):
+    b = W.make_batch([10, 0, 50], [40, 0, 25], 8, 2, 64, "f16", window=20,
+                     sink_mode="smooth", seed=77)
+    # 9 trailing q rows that belong to no sequence
+    pad = torch.randn(9, 8, 64).to(torch.float16)
+    padded = W.Batch(torch.cat([b.q, pad]), b.k, b.v, b.cu_seqlens_q, b.prefix_lens,
+                     b.kv_indptr, b.hq, b.hkv, b.d, b.window, b.sinks, b.smooth, b.scale)
+    out, lse = run_gpu(pkg, padded)
+    assert torch.isnan(out[65:].float()).all() and torch.isnan(lse[65:]).all()
+    ref, ref_lse = run_oracle(b)
+    compare(out[:65], lse[:65], ref, ref_lse, label="padded")
+
+
+def test_run_to_run_bitwise(pkg):
+    b = W.make_batch([100, 0], [333, 129], 64, 8, 64, "bf16", window=128,
+                     sink_mode="head", seed=9)
+    o1, l1 = run_gpu(pkg, b)
+    o2, l2 = run_gpu(pkg, b)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+
+
+def test_bad_metadata_is_reported(pkg):
+    b = W.make_batch([5, 6], [20, 30], 8, 2, 64, "bf16", window=0, sink_mode="none", seed=3)
+    dev = b.to("cuda")
+    bad_kv = dev.kv_indptr.clone()
+    bad_kv[1] += 1  # spans no longer equal prefix + extend
+    out = torch.full_like(dev.q, 7.0)
+    pkg.gqa_flash_prefill(dev.q, dev.k, dev.v, dev.cu_seqlens_q, dev.prefix_lens, bad_kv,
+                          dev.scale, out=out)
+    torch.cuda.synchronize()
+    assert pkg.get_device_status() == pkg.GQA_DEV_BAD_METADATA
+    assert bool((out == 7.0).all())
+    assert pkg.get_device_status() == 0  # cleared by the read
+
+
+# ------------------------------------------------------------- tile bookkeeping
+
+def _bookkeeping(pkg, batch):
+    p = pkg.plan(batch.num_seqs, batch.total_q, batch.max_seqlen_q, batch.hq, batch.hkv,
+                 batch.d, batch.dtype_name, batch.window)
+    log = torch.full((p["max_units"], 8), -1, dtype=torch.int32, device="cuda")
+    run_gpu(pkg, batch, debug_log=log)
+    log = log.cpu().numpy()
+    used = log[log[:, 0] >= 0]
+    want = oracle.tile_census(batch.cu_seqlens_q, batch.prefix_lens, batch.hkv,
+                              p["rows_per_unit"], p["block_n"], batch.window)
+    got = used[np.lexsort((used[:, 2], used[:, 1], used[:, 0]))][:, :6]
+    assert got.shape == want.shape, (got.shape, want.shape)
+    assert np.array_equal(got, want)
+    # every unit ran exactly once, on some CTA, in that CTA's order
+    assert len(used) == len(want)
+    return p, used
+
+
+@pytest.mark.parametrize("window", [0, 1, 15, 100, 128, 129, 4096])
+def test_bookkeeping_bit_exact_ragged(pkg, window):
+    b = W.make_batch([0, 37, 5000, 129, 64], [1, 300, 700, 128, 129], 64, 8, 64, "bf16",
+                     window=window, sink_mode="head", seed=window + 1)
+    _bookkeeping(pkg, b)
+
+
+def test_bookkeeping_full_size_layer_pair(pkg):
+    for b in W.layer_pair(seq=4096, seed=1):
+        _bookkeeping(pkg, b)
+
+
+def test_window_cost_flat_in_prefix(pkg):
+    """Tiles walked per unit stop growing with the prefix once the window is
+    filled (hip-ep PR #622 window commit; SGLang PR #34468 commit 1)."""
+    per_unit = []
+    for prefix in (0, 512, 8192, 16384):
+        b = W.make_batch([prefix], [512], 64, 8, 64, "bf16", window=128,
+                         sink_mode="head", seed=prefix + 1)
+        p, used = _bookkeeping(pkg, b)
+        per_unit.append(int(used[:, 4].max()))
+    bound = -(-(128 + p["rows_per_unit"] - 1) // p["block_n"]) + 1
+    assert max(per_unit) <= bound, (per_unit, bound)
+    assert per_unit[1:] == [per_unit[1]] * 3
+
+
+# ------------------------------------------------------------- full sizes, sampled rows
+
+def test_layer_pair_full_size_sampled(pkg):
+    for b in W.layer_pair(seq=4096, seed=1):
+        _check_sampled(pkg, b, sample_rows(b, per_seq=160, seed=1))
+
+
+@pytest.mark.parametrize("layout", ["window-bounded", "full-prefix"])
+def test_chunked_prefix_full_size_sampled(pkg, layout):
+    full = W.chunked_prefix(num_seqs=8, prefix=8192, extend=8192, window=128, seed=2)
+    b = W.window_bounded(full, 128) if layout == "window-bounded" else full
+    out, lse = run_gpu(pkg, b)
+    seqs = [0, 5]
+    sb = sub_batch(b, seqs)
+    rows_sb = sample_rows(sb, per_seq=40, seed=3)
+    ref, ref_lse = run_oracle(sb, rows=rows_sb)
+    cu = b.cu_seqlens_q.tolist()
+    # map sub-batch rows back to the full batch's rows
+    scu = sb.cu_seqlens_q.tolist()
+    back = np.concatenate([np.arange(cu[s], cu[s + 1]) for s in seqs])
+    compare(out[back], lse[back], ref, ref_lse, rows=rows_sb, label=layout)
+
+
+@pytest.mark.parametrize("layer", [0, 1])
+@pytest.mark.parametrize("chunk", [0, 1, 17, 31])
+def test_oss20b_chunks_sampled(pkg, layer, chunk):
+    b = W.oss20b_chunk(layer, chunk)
+    _check_sampled(pkg, b, sample_rows(b, per_seq=48, seed=chunk))
+
+
+RAGGED_CELLS = [
+    (64, 8, 64, 128, "head", "bf16"),
+    (32, 4, 128, 0, "smooth", "f16"),
+    (64, 8, 256, 1, "none", "bf16"),
+    (32, 4, 64, 4096, "head", "f16"),
+    (64, 8, 128, 127, "head", "bf16"),
+    (32, 4, 256, 129, "smooth", "bf16"),
+]
+
+
+@pytest.mark.parametrize("hq,hkv,d,window,sink,dtype", RAGGED_CELLS)
+def test_ragged_full_size_sampled(pkg, hq, hkv, d, window, sink, dtype):
+    b = W.ragged(hq=hq, hkv=hkv, d=d, dtype=dtype, window=window, sink_mode=sink,
+                 seed=4)
+    out, lse = run_gpu(pkg, b)
+    seqs = [0, 7, 15]
+    sb = sub_batch(b, seqs)
+    rows_sb = sample_rows(sb, per_seq=12, seed=5)
+    ref, ref_lse = run_oracle(sb, rows=rows_sb)
+    cu = b.cu_seqlens_q.tolist()
+    back = np.concatenate([np.arange(cu[s], cu[s + 1]) for s in seqs])
+    compare(out[back], lse[back], ref, ref_lse, rows=rows_sb, label=b.name)
+    # every row of every sequence was written with finite values
+    assert torch.isfinite(out.float()).all()
+
+
+# ------------------------------------------------------------- exact key sets
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("window", [0, 1, 15, 64, 100, 129])
+def test_counting_probe_exact_key_sets(pkg, dtype, window):
+    """q = 0 makes every kept probability exactly 1, so lse = ln(n) and, with
+    v[j, c] = [j mod 64 == c], out[c] * n counts the kept keys in each residue
+    class: integers recovered exactly pin every row's key set."""
+    b = W.make_batch([0, 300, 1000, 63], [200, 129, 64, 70], 16, 2, 64, dtype,
+                     window=window, sink_mode="none", seed=window)
+    b.q.zero_()
+    j = torch.arange(b.total_kv) - torch.repeat_interleave(
+        b.kv_indptr[:-1], torch.diff(b.kv_indptr))
+    b.v.zero_()
+    b.v[torch.arange(b.total_kv), :, j % 64] = 1.0
+    out, lse = run_gpu(pkg, b)
+    n = torch.exp(lse.double()).round().long()
+    counts = (out.double() * n[..., None]).round().long()
+    cu, pre = b.cu_seqlens_q.tolist(), b.prefix_lens.tolist()
+    for s in range(b.num_seqs):
+        for i in range(cu[s + 1] - cu[s]):
+            pos = pre[s] + i
+            lo = 0 if window <= 0 else max(0, pos - window + 1)
+            want_n = pos - lo + 1
+            want = torch.bincount(torch.arange(lo, pos + 1) % 64, minlength=64)
+            row = cu[s] + i
+            assert bool((n[row] == want_n).all()), (s, i, n[row], want_n)
+            assert bool((counts[row] == want).all()), (s, i)
