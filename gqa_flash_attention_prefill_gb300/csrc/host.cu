@@ -94,9 +94,11 @@ int pow2_bucket(int x) {
   return b;
 }
 
+// Measured on GB300 (gpt-oss layer pair and chunked-prefix workloads): a
+// full-causal d=64 layer runs fastest with 128-key tiles; windowed layers with
+// 64-key tiles, which waste fewer masked keys at the window's lower edge.
 int default_block_n(int d, bool windowed) {
-  (void)windowed;
-  if (d == 64) return 128;
+  if (d == 64) return windowed ? 64 : 128;
   return 64;
 }
 

@@ -66,9 +66,13 @@ __host__ __device__ constexpr int tmem_cols_for(int D, int BN) {
                                     : 512;
 }
 
+// Q tiles in flight per CTA: two (the next unit's Q loads during the current
+// unit) where shared memory allows, one for d = 256.
+__host__ __device__ constexpr int q_buffers(int D) { return D >= 256 ? 1 : 2; }
+
 __host__ __device__ constexpr uint32_t smem_bytes_for(int D, int BN, int NS) {
   return 1024u                                  // alignment slack
-         + 128u * D * 2u                        // Q tile
+         + (uint32_t)q_buffers(D) * 128u * D * 2u  // Q tiles
          + 2u * NS * BN * D * 2u                // K and V rings
          + 64u * 8u                             // mbarriers
          + 16u                                  // misc words
@@ -78,11 +82,11 @@ __host__ __device__ constexpr uint32_t smem_bytes_for(int D, int BN, int NS) {
 // Barrier indices
 template <int NS>
 struct Bar {
-  static constexpr int kQFull = 0, kQEmpty = 1;
-  static constexpr int kKFull = 2, kKEmpty = 2 + NS, kVFull = 2 + 2 * NS, kVEmpty = 2 + 3 * NS;
-  static constexpr int kSFull = 2 + 4 * NS, kSFree = kSFull + 1, kPFull = kSFull + 2;
-  static constexpr int kODone = kSFull + 3, kOFree = kSFull + 4, kDrain = kSFull + 5;
-  static constexpr int kCount = kSFull + 6;
+  static constexpr int kQFull = 0, kQEmpty = 2;  // two each (Q double buffer)
+  static constexpr int kKFull = 4, kKEmpty = 4 + NS, kVFull = 4 + 2 * NS, kVEmpty = 4 + 3 * NS;
+  static constexpr int kSFull = 4 + 4 * NS, kSFree = kSFull + 1, kPFull = kSFull + 2;
+  static constexpr int kODone = kSFull + 3, kDrain = kSFull + 4;
+  static constexpr int kCount = kSFull + 5;
 };
 
 struct Unit {
@@ -184,10 +188,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t sQ = smem_u32(smem);
-  const uint32_t sK = sQ + kQBytes;
+  constexpr uint32_t NQ = (uint32_t)q_buffers(D);
+  const uint32_t sQ = smem_u32(smem);  // NQ Q buffers
+  const uint32_t sK = sQ + NQ * kQBytes;
   const uint32_t sV = sK + NS * kKVBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQBytes + 2 * NS * kKVBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NQ * kQBytes + 2 * NS * kKVBytes);
   const uint32_t sBar = smem_u32(bars);
   uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 64);  // [0] tmem base, [1] abort, [2] bad
   int32_t* tile_start = reinterpret_cast<int32_t*>(misc + 4);
@@ -231,21 +236,28 @@ __global__ void __launch_bounds__(kThreads, MINB)
     else
       local += (E + p.rows - 1) / p.rows;
   }
-  scan[tid] = local;
   if (bad) misc[2] = 1u;
+  // Exclusive scan of the per-thread counts: warp scans, then warp totals.
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) scan[warp] = incl;
   __syncthreads();
   if (tid == 0) {
     int acc = 0;
-    for (int i = 0; i < kThreads; ++i) {
-      const int v = scan[i];
-      scan[i] = acc;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      const int v = scan[w];
+      scan[w] = acc;
       acc += v;
     }
     tile_start[nseq] = acc;
   }
   __syncthreads();
   {
-    int acc = scan[tid];
+    int acc = scan[warp] + incl - local;
     for (int b = b_lo; b < b_hi; ++b) {
       tile_start[b] = acc;
       const int E = __ldg(p.cu_seqlens_q + b + 1) - __ldg(p.cu_seqlens_q + b);
@@ -270,22 +282,37 @@ __global__ void __launch_bounds__(kThreads, MINB)
   const uint32_t tmem = misc[0];
 
   // ---------------------------------------------------------------- producer
+  // With two Q buffers the next unit's Q tile is requested right after the
+  // current unit's first K/V tile, so its load overlaps the current unit; with
+  // one, after the last K/V tile (its buffer frees when that unit's last
+  // QK^T completes).
   if (warp == 4) {
     if (lane == 0) {
-      uint32_t it = 0, uc = 0, nk[NS], nv[NS];
+      uint32_t it = 0, nq = 0, nk[NS], nv[NS];
       for (int s = 0; s < NS; ++s) nk[s] = nv[s] = 0u;
       bool ok = true;
-      for (int k = 0; ok; ++k) {
-        const int u = unit_of(k);
-        if (u >= n_units) break;
-        const Unit U = decode_unit(p, tile_start, u, BN);
-        if (!(ok = wait_bounded(sBar + 8u * B::kQEmpty, (uc & 1u) ^ 1u, abort_flag, p.status, tmo)))
-          break;
-        mbar_arrive_expect_tx(sBar + 8u * B::kQFull, kQBytes);
+      auto issue_q = [&](const Unit& U) -> bool {
+        const uint32_t qb = nq % NQ;
+        if (!wait_bounded(sBar + 8u * (B::kQEmpty + qb), ((nq / NQ) & 1u) ^ 1u, abort_flag,
+                          p.status, tmo))
+          return false;
+        mbar_arrive_expect_tx(sBar + 8u * (B::kQFull + qb), kQBytes);
         for (int c = 0; c < NCH; ++c)
-          tma_load_3d(sQ + c * kQChunk, &p.tmap_q, sBar + 8u * B::kQFull, c * 64, U.g * p.G,
-                      U.q_row0);
-        ++uc;
+          tma_load_3d(sQ + qb * kQBytes + c * kQChunk, &p.tmap_q, sBar + 8u * (B::kQFull + qb),
+                      c * 64, U.g * p.G, U.q_row0);
+        ++nq;
+        return true;
+      };
+      int k = 0;
+      int u = unit_of(0);
+      Unit U;
+      if (u < n_units) {
+        U = decode_unit(p, tile_start, u, BN);
+        ok = issue_q(U);
+      }
+      while (ok && u < n_units) {
+        const int u_next = unit_of(k + 1);
+        Unit Un;
         for (int j = 0; j < U.n_tiles; ++j, ++it) {
           const uint32_t s = it % NS, ph = (it / NS) & 1u;
           const int row = U.kv_base + U.kv_lo + j * BN;
@@ -303,10 +330,22 @@ __global__ void __launch_bounds__(kThreads, MINB)
             tma_load_3d(sV + s * kKVBytes + c * kKVChunk, &p.tmap_v, sBar + 8u * (B::kVFull + s),
                         c * 64, U.g, row);
           ++nv[s];
+          if (j == (NQ == 2 ? 0 : U.n_tiles - 1) && u_next < n_units) {
+            Un = decode_unit(p, tile_start, u_next, BN);
+            if (!(ok = issue_q(Un))) break;
+          }
         }
+        ++k;
+        u = u_next;
+        U = Un;
       }
       // Let every copy issued land before the CTA can exit.
-      if (uc > 0) wait_drain(sBar + 8u * B::kQFull, (uc - 1u) & 1u, tmo);
+      for (uint32_t b = 0; b < NQ; ++b) {
+        if (nq > b) {
+          const uint32_t last = nq - 1u - b;  // the last load into buffer (last % NQ)
+          wait_drain(sBar + 8u * (B::kQFull + last % NQ), (last / NQ) & 1u, tmo);
+        }
+      }
       for (int s = 0; s < NS; ++s) {
         if (nk[s] > 0) wait_drain(sBar + 8u * (B::kKFull + s), (nk[s] - 1u) & 1u, tmo);
         if (nv[s] > 0) wait_drain(sBar + 8u * (B::kVFull + s), (nv[s] - 1u) & 1u, tmo);
@@ -321,8 +360,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
       // Q and K: K-major, 128-byte swizzle; the 16-wide k-step advances the
       // start address by 32 bytes inside a 128-byte swizzle row, the 64-wide
       // d-chunk by one chunk.  Stride between 8-row groups: 1024 bytes.
-      auto qdesc = [&](int kk) {
-        return smem_desc_sw128(sQ + (kk >> 2) * kQChunk + (kk & 3) * 32, 16, 1024);
+      auto qdesc = [&](uint32_t qb, int kk) {
+        return smem_desc_sw128(sQ + qb * kQBytes + (kk >> 2) * kQChunk + (kk & 3) * 32, 16, 1024);
       };
       auto kdesc = [&](uint32_t s, int kk) {
         return smem_desc_sw128(sK + s * kKVBytes + (kk >> 2) * kKVChunk + (kk & 3) * 32, 16, 1024);
@@ -351,7 +390,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
         const int u = unit_of(k);
         if (u >= n_units) break;
         const Unit U = decode_unit(p, tile_start, u, BN);
-        if (!(ok = wait_bounded(sBar + 8u * B::kQFull, uc & 1u, abort_flag, p.status, tmo))) break;
+        const uint32_t qb = uc % NQ;
+        if (!(ok = wait_bounded(sBar + 8u * (B::kQFull + qb), (uc / NQ) & 1u, abort_flag, p.status,
+                                tmo)))
+          break;
         for (int j = 0; j < U.n_tiles; ++j) {
           const uint32_t cur = it + j;
           const uint32_t s = cur % NS, ph = (cur / NS) & 1u;
@@ -362,10 +404,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + kColS, qdesc(kk), kdesc(s, kk), kIdescS, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + kColS, qdesc(qb, kk), kdesc(s, kk), kIdescS, kk > 0 ? 1u : 0u);
           mma_commit(sBar + 8u * B::kSFull);
           mma_commit(sBar + 8u * (B::kKEmpty + s));
-          if (j == U.n_tiles - 1) mma_commit(sBar + 8u * B::kQEmpty);
+          if (j == U.n_tiles - 1) mma_commit(sBar + 8u * (B::kQEmpty + qb));
           // PV of the previous tile goes after this tile's QK^T, so the
           // tensor core works on S(j) while the softmax warps work on S(j-1).
           if (j > 0 && !(ok = issue_pv(cur - 1u, j == 1))) break;
@@ -403,47 +445,80 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         wait_bounded(sBar + 8u * B::kSFull, it & 1u, abort_flag, p.status, tmo));
         if (!ok) break;
         tc_fence_after();
-        uint32_t sr[BN];
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c)
-          tmem_ld32(t_lane + kColS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(sBar + 8u * B::kSFree);  // S is in registers: next QK^T may overwrite it
-
-        // Per-element mask, edge tiles only (the decision is uniform over the CTA).
-        if (tile_needs_mask(n0, BN, U.P, U.q0, U.q_last, win)) {
-          ++n_masked;
-          const int lo = pos - win + 1;
-#pragma unroll
-          for (int c = 0; c < BN; ++c) {
-            const int key = n0 + c;
-            if (key > pos || (WIN && key < lo)) sr[c] = __float_as_uint(-INFINITY);
-          }
-        }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < BN; c += 2)
-          mx = max3(mx, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-        const float m_cand = mx * sl2;
-        const bool upd = m_cand > m + kRescaleThreshold;
-        const float m_new = upd ? m_cand : m;
-        const float alpha = upd ? ex2(m - m_new) : 1.f;
-        // NaN guard: a row that has seen no key keeps m = -inf; its scores
-        // are all -inf, and with a zero offset every probability is exactly 0.
-        const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
-        float sum0 = 0.f, sum1 = 0.f;
+        // The S row is processed in 64-column chunks so that only one chunk
+        // of fp32 scores is live in registers; the packed 16-bit P of earlier
+        // chunks (half the size) waits in registers until the tile is done.
+        const bool edge = tile_needs_mask(n0, BN, U.P, U.q0, U.q_last, win);
+        n_masked += edge ? 1 : 0;
         uint32_t pk[BN / 2];
+        float alpha = 1.f;  // product of this tile's reference moves
+        bool upd_any = false;
 #pragma unroll
-        for (int c = 0; c < BN; c += 2) {
-          const float p0 = ex2(fmaf(__uint_as_float(sr[c]), sl2, neg_m));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), sl2, neg_m));
-          sum0 += p0;
-          sum1 += p1;
-          pk[c / 2] = pack2<BF16>(p0, p1);
+        for (int ch = 0; ch < BN / 64; ++ch) {
+          uint32_t sr[64];
+          tmem_ld32(t_lane + kColS + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(sr));
+          tmem_ld32(t_lane + kColS + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+          tmem_wait_ld();
+          if (ch == BN / 64 - 1) {
+            tc_fence_before();
+            mbar_arrive(sBar + 8u * B::kSFree);  // S is in registers: next QK^T may overwrite it
+          }
+          // Per-element mask, edge tiles only (uniform over the CTA): row
+          // `pos` keeps columns [c_lo, c_hi] of this chunk.
+          if (edge) {
+            const int c_hi = pos - (n0 + ch * 64);
+            const int c_lo = WIN ? pos - win + 1 - (n0 + ch * 64) : -1;
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (c > c_hi || c < c_lo) sr[c] = __float_as_uint(-INFINITY);
+          }
+          // Chunk max over independent chains (short dependency chains).
+          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 64; c += 8) {
+            mx0 = max3(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
+            mx1 = max3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+            mx2 = max3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+            mx3 = max3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+          }
+          const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+          if (m_cand > m + kRescaleThreshold) {  // move the reference (rare after the first tile)
+            const float a = ex2(m - m_cand);     // m = -inf gives 0
+            alpha *= a;
+            l *= a;
+            m = m_cand;
+            upd_any = true;
+#pragma unroll
+            for (int i = 0; i < ch * 32; ++i) {  // earlier chunks of this tile
+              const float lo = unpack_lo<BF16>(pk[i]) * a, hi = unpack_hi<BF16>(pk[i]) * a;
+              pk[i] = pack2<BF16>(lo, hi);
+            }
+          }
+          // NaN guard: a row that has seen no key keeps m = -inf; its scores
+          // are all -inf, and with a zero offset every probability is exactly 0.
+          const float neg_m = (m == -INFINITY) ? 0.f : -m;
+          const uint64_t sc2 = f2(sl2, sl2), nm2 = f2(neg_m, neg_m);
+          uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;  // packed partial sums
+#pragma unroll
+          for (int c = 0; c < 64; c += 8) {
+            float x[8];
+#pragma unroll
+            for (int t = 0; t < 8; t += 2)
+              unf2(ffma2(f2(__uint_as_float(sr[c + t]), __uint_as_float(sr[c + t + 1])), sc2, nm2),
+                   x[t], x[t + 1]);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) x[t] = ex2(x[t]);
+            acc0 = fadd2(acc0, f2(x[0], x[1]));
+            acc1 = fadd2(acc1, f2(x[2], x[3]));
+            acc2 = fadd2(acc2, f2(x[4], x[5]));
+            acc3 = fadd2(acc3, f2(x[6], x[7]));
+#pragma unroll
+            for (int t = 0; t < 8; t += 2) pk[ch * 32 + (c + t) / 2] = pack2<BF16>(x[t], x[t + 1]);
+          }
+          float r0, r1;
+          unf2(fadd2(fadd2(acc0, acc1), fadd2(acc2, acc3)), r0, r1);
+          l += r0 + r1;
         }
-        l = l * alpha + (sum0 + sum1);
-        m = m_new;
 
         // P and O are touched only once the previous PV has finished.
         if (it > 0)
@@ -454,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
 #pragma unroll
         for (int c = 0; c < BN / 64; ++c)
           tmem_st32(t_lane + kColP + c * 32, *reinterpret_cast<uint32_t(*)[32]>(pk + c * 32));
-        const bool corr = upd && j > 0;
+        const bool corr = upd_any && j > 0;
         if (__any_sync(0xffffffffu, corr)) {
           const float a = corr ? alpha : 1.f;
 #pragma unroll 1

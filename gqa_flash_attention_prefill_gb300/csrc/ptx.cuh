@@ -3,6 +3,7 @@
 // Written from the public PTX ISA descriptions of these instructions.
 #pragma once
 #include <cstdint>
+#include <cuda_fp16.h>
 
 namespace gqa {
 
@@ -175,5 +176,45 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// The two halves of a 16-bit pair as fp32 (exact).
+template <bool BF16>
+__device__ __forceinline__ float unpack_lo(uint32_t v) {
+  if constexpr (BF16) return __uint_as_float(v << 16);
+  __half h = __ushort_as_half((unsigned short)(v & 0xFFFFu));
+  return __half2float(h);
+}
+template <bool BF16>
+__device__ __forceinline__ float unpack_hi(uint32_t v) {
+  if constexpr (BF16) return __uint_as_float(v & 0xFFFF0000u);
+  __half h = __ushort_as_half((unsigned short)(v >> 16));
+  return __half2float(h);
+}
 
+}  // namespace gqa
+
+namespace gqa {
+// Packed pairs of fp32 (sm_100+ f32x2 arithmetic: two lanes per instruction).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unf2(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 }  // namespace gqa
