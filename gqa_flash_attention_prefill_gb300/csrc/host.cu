@@ -12,7 +12,7 @@
 #include <mutex>
 #include <tuple>
 
-#include "../../include/gqa_prefill.h"
+#include "gqa_prefill.h"
 #include "launch.h"
 
 namespace gqa {

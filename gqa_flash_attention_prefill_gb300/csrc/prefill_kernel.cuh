@@ -57,13 +57,17 @@ struct PrefillParams {
   unsigned long long timeout_ns;
 };
 
+__host__ __device__ constexpr int pow2_cols(int n) {
+  return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512;
+}
+// P buffers in tensor memory: two when the allocation does not grow (then
+// the softmax of tile j only waits for the PV of tile j-2), else one.
+__host__ __device__ constexpr int p_buffers(int D, int BN) {
+  return pow2_cols(BN + BN + D) == pow2_cols(BN + BN / 2 + D) ? 2 : 1;
+}
+// S (BN fp32 columns) + P buffers (BN 16-bit values = BN/2 columns each) + O (D columns)
 __host__ __device__ constexpr int tmem_cols_for(int D, int BN) {
-  // S (BN fp32 columns) + P (BN 16-bit values = BN/2 columns) + O (D columns)
-  return (BN + BN / 2 + D) <= 32 ? 32
-         : (BN + BN / 2 + D) <= 64 ? 64
-         : (BN + BN / 2 + D) <= 128 ? 128
-         : (BN + BN / 2 + D) <= 256 ? 256
-                                    : 512;
+  return pow2_cols(BN + p_buffers(D, BN) * (BN / 2) + D);
 }
 
 // Q tiles in flight per CTA: two (the next unit's Q loads during the current
@@ -84,9 +88,10 @@ template <int NS>
 struct Bar {
   static constexpr int kQFull = 0, kQEmpty = 2;  // two each (Q double buffer)
   static constexpr int kKFull = 4, kKEmpty = 4 + NS, kVFull = 4 + 2 * NS, kVEmpty = 4 + 3 * NS;
-  static constexpr int kSFull = 4 + 4 * NS, kSFree = kSFull + 1, kPFull = kSFull + 2;
-  static constexpr int kODone = kSFull + 3, kDrain = kSFull + 4;
-  static constexpr int kCount = kSFull + 5;
+  static constexpr int kSFull = 4 + 4 * NS, kSFree = kSFull + 1;
+  static constexpr int kPFull = kSFull + 2, kODone = kSFull + 4;  // one per P buffer
+  static constexpr int kDrain = kSFull + 6;
+  static constexpr int kCount = kSFull + 7;
 };
 
 struct Unit {
@@ -180,7 +185,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
   constexpr uint32_t kQChunk = 128u * 128u;
   constexpr uint32_t kKVChunk = (uint32_t)BN * 128u;
   constexpr uint32_t kTmemCols = (uint32_t)tmem_cols_for(D, BN);
-  constexpr uint32_t kColS = 0, kColP = BN, kColO = BN + BN / 2;
+  constexpr uint32_t NP = (uint32_t)p_buffers(D, BN);
+  constexpr uint32_t kColS = 0, kColP = BN, kColO = BN + NP * (BN / 2);
   constexpr uint32_t kIdescS = idesc_f16(BF16, 128, BN, false);  // Q, K both K-major
   constexpr uint32_t kIdescO = idesc_f16(BF16, 128, D, true);    // V is MN-major
   using B = Bar<NS>;
@@ -206,7 +212,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
   // ---------------------------------------------------------------- set-up
   if (tid == 0) {
     for (int i = 0; i < B::kCount; ++i)
-      mbar_init(sBar + 8u * i, (i == B::kSFree || i == B::kPFull) ? 128u : 1u);
+      mbar_init(sBar + 8u * i,
+                (i == B::kSFree || i == B::kPFull || i == B::kPFull + 1) ? 128u : 1u);
     misc[1] = 0u;
     misc[2] = 0u;
     fence_barrier_init();
@@ -374,13 +381,15 @@ __global__ void __launch_bounds__(kThreads, MINB)
       auto issue_pv = [&](uint32_t itp, bool first) -> bool {
         const uint32_t sp = itp % NS, php = (itp / NS) & 1u;
         if (!wait_bounded(sBar + 8u * (B::kVFull + sp), php, abort_flag, p.status, tmo)) return false;
-        if (!wait_bounded(sBar + 8u * B::kPFull, itp & 1u, abort_flag, p.status, tmo)) return false;
+        const uint32_t pb = itp % NP;
+        if (!wait_bounded(sBar + 8u * (B::kPFull + pb), (itp / NP) & 1u, abort_flag, p.status, tmo))
+          return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem + kColO, tmem + kColP + kk * 8, vdesc(sp, kk), kIdescO,
+          mma_ts(tmem + kColO, tmem + kColP + pb * (BN / 2) + kk * 8, vdesc(sp, kk), kIdescO,
                  (first && kk == 0) ? 0u : 1u);
-        mma_commit(sBar + 8u * B::kODone);
+        mma_commit(sBar + 8u * (B::kODone + pb));
         mma_commit(sBar + 8u * (B::kVEmpty + sp));
         return true;
       };
@@ -520,17 +529,29 @@ __global__ void __launch_bounds__(kThreads, MINB)
           l += r0 + r1;
         }
 
-        // P and O are touched only once the previous PV has finished.
-        if (it > 0)
-          ok = __all_sync(0xffffffffu, wait_bounded(sBar + 8u * B::kODone, (it - 1u) & 1u,
-                                                     abort_flag, p.status, tmo));
+        // P buffer `pb` is rewritten once the PV that last read it is done.
+        const uint32_t pb = it % NP;
+        if (it >= NP)
+          ok = __all_sync(0xffffffffu, wait_bounded(sBar + 8u * (B::kODone + pb),
+                                                     ((it / NP) & 1u) ^ 1u, abort_flag, p.status,
+                                                     tmo));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < BN / 64; ++c)
-          tmem_st32(t_lane + kColP + c * 32, *reinterpret_cast<uint32_t(*)[32]>(pk + c * 32));
+          tmem_st32(t_lane + kColP + pb * (BN / 2) + c * 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(pk + c * 32));
         const bool corr = upd_any && j > 0;
         if (__any_sync(0xffffffffu, corr)) {
+          // Rescaling O needs every earlier PV done (PVs complete in order).
+          if (NP > 1) {
+            const uint32_t prev = it - 1u;
+            ok = __all_sync(0xffffffffu,
+                            wait_bounded(sBar + 8u * (B::kODone + prev % NP), (prev / NP) & 1u,
+                                         abort_flag, p.status, tmo));
+            if (!ok) break;
+            tc_fence_after();
+          }
           const float a = corr ? alpha : 1.f;
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
@@ -544,13 +565,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(sBar + 8u * B::kPFull);
+        mbar_arrive(sBar + 8u * (B::kPFull + pb));
       }
       if (!ok) break;
 
       // Epilogue: fold the sink into the denominator, normalise, store.
-      ok = __all_sync(0xffffffffu, wait_bounded(sBar + 8u * B::kODone, (it - 1u) & 1u, abort_flag,
-                                                 p.status, tmo));
+      ok = __all_sync(0xffffffffu, wait_bounded(sBar + 8u * (B::kODone + (it - 1u) % NP),
+                                                 ((it - 1u) / NP) & 1u, abort_flag, p.status, tmo));
       if (!ok) break;
       tc_fence_after();
       const bool has_x = (p.sinks != nullptr) || (p.smooth != 0);
@@ -570,18 +591,19 @@ __global__ void __launch_bounds__(kThreads, MINB)
       const size_t orow = (size_t)(U.q_row0 + r / p.G) * p.Hq + h;
       uint16_t* op = reinterpret_cast<uint16_t*>(p.out) + orow * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(t_lane + kColO + c * 32, o);
+      for (int c = 0; c < D / 64; ++c) {  // 64 columns per round trip
+        uint32_t o[64];
+        tmem_ld32(t_lane + kColO + c * 64, *reinterpret_cast<uint32_t(*)[32]>(o));
+        tmem_ld32(t_lane + kColO + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
         tmem_wait_ld();
         if (valid) {
-          uint32_t w[16];
+          uint32_t w[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
+          for (int i = 0; i < 32; ++i)
             w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(op + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(op + c * 64);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
+          for (int i = 0; i < 8; ++i)
             dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
       }
