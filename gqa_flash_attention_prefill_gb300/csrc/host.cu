@@ -207,6 +207,7 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q
   rc = encode_map(&p.tmap_q, q, dtype, d, Hq, total_q, pl.G, pl.rows);
   if (rc == GQA_OK) rc = encode_map(&p.tmap_k, k, dtype, d, Hkv, total_kv, 1, pl.shape.block_n);
   if (rc == GQA_OK) rc = encode_map(&p.tmap_v, v, dtype, d, Hkv, total_kv, 1, pl.shape.block_n);
+  if (rc == GQA_OK) rc = encode_map(&p.tmap_o, out, dtype, d, Hq, total_q, pl.G, pl.rows);
   if (rc != GQA_OK) return rc;
   p.cu_seqlens_q = cu_seqlens_q;
   p.prefix_lens = prefix_lens;
@@ -258,7 +259,7 @@ bool kernel_shape(int d, int block_n, KernelShape* out) {
   KernelShape s;
   s.block_n = block_n;
   if (d == 64 && block_n == 128) { s.kv_stages = 2; s.min_blocks = 2; }
-  else if (d == 64 && block_n == 64) { s.kv_stages = 3; s.min_blocks = 2; }
+  else if (d == 64 && block_n == 64) { s.kv_stages = 4; s.min_blocks = 2; }
   else if (d == 128 && block_n == 64) { s.kv_stages = 2; s.min_blocks = 2; }
   else if (d == 128 && block_n == 128) { s.kv_stages = 2; s.min_blocks = 1; }
   else if (d == 256 && block_n == 64) { s.kv_stages = 2; s.min_blocks = 1; }

@@ -27,7 +27,7 @@
 
 namespace gqa {
 
-constexpr int kMaxSeqs = 1024;       // sequences per call (smem tile table)
+constexpr int kMaxSeqs = 512;        // sequences per call (shared-memory tables)
 constexpr int kThreads = 192;        // 6 warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -41,6 +41,7 @@ struct PrefillParams {
   CUtensorMap tmap_q;  // [total_q, Hq, d]  box (64, G, 128/G), 128B swizzle
   CUtensorMap tmap_k;  // [total_kv, Hkv, d] box (64, 1, BN)
   CUtensorMap tmap_v;
+  CUtensorMap tmap_o;  // out, same geometry as tmap_q (TMA store of full units)
   const int32_t* cu_seqlens_q;
   const int32_t* prefix_lens;
   const int32_t* kv_indptr;
@@ -70,9 +71,9 @@ __host__ __device__ constexpr int tmem_cols_for(int D, int BN) {
   return pow2_cols(BN + p_buffers(D, BN) * (BN / 2) + D);
 }
 
-// Q tiles in flight per CTA: two (the next unit's Q loads during the current
-// unit) where shared memory allows, one for d = 256.
-__host__ __device__ constexpr int q_buffers(int D) { return D >= 256 ? 1 : 2; }
+// Q tiles in flight per CTA: two for d = 64 (the next unit's Q loads during
+// the current unit and two CTAs still fit on an SM), one for larger d.
+__host__ __device__ constexpr int q_buffers(int D) { return D == 64 ? 2 : 1; }
 
 __host__ __device__ constexpr uint32_t smem_bytes_for(int D, int BN, int NS) {
   return 1024u                                  // alignment slack
@@ -80,7 +81,8 @@ __host__ __device__ constexpr uint32_t smem_bytes_for(int D, int BN, int NS) {
          + 2u * NS * BN * D * 2u                // K and V rings
          + 64u * 8u                             // mbarriers
          + 16u                                  // misc words
-         + 4u * (kMaxSeqs + 1) + 4u * kThreads; // tile table + scan scratch
+         + 4u * (4 * kMaxSeqs + 2)              // per-sequence tables
+         + 4u * 8u;                             // scan scratch (one word per warp)
 }
 
 // Barrier indices
@@ -91,36 +93,46 @@ struct Bar {
   static constexpr int kSFull = 4 + 4 * NS, kSFree = kSFull + 1;
   static constexpr int kPFull = kSFull + 2, kODone = kSFull + 4;  // one per P buffer
   static constexpr int kDrain = kSFull + 6;
-  static constexpr int kCount = kSFull + 7;
+  static constexpr int kEpi = kSFull + 7;  // output tile staged in shared memory
+  static constexpr int kCount = kSFull + 8;
 };
 
 struct Unit {
   int b, g, q0, q_last, P, E, kv_base, q_row0, kv_lo, n_tiles;
 };
 
+// Per-sequence metadata copied into shared memory once per CTA, so that
+// decoding a unit never waits on global memory.
+struct SeqTab {
+  const int32_t* tile_start;  // [B+1] exclusive scan of query tiles per sequence
+  const int32_t* cu0;         // [B+1] cu_seqlens_q
+  const int32_t* pre;         // [B]   prefix_lens
+  const int32_t* kvb;         // [B]   kv_indptr (first key row)
+};
+
 // Unit u -> (sequence, KV head, query tile).  Units are numbered with the KV
 // head fastest and, inside a sequence, the last (costliest under causality)
 // query tile first.
-__device__ __forceinline__ Unit decode_unit(const PrefillParams& p, const int32_t* tile_start,
-                                            int u, int BN) {
+__device__ __forceinline__ Unit decode_unit(const PrefillParams& p, const SeqTab& T, int u,
+                                            int BN) {
   Unit U;
   U.g = u % p.Hkv;
   const int tau = u / p.Hkv;
   int lo = 0, hi = p.num_seqs;  // find b with tile_start[b] <= tau < tile_start[b+1]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (tile_start[mid] <= tau) lo = mid; else hi = mid;
+    if (T.tile_start[mid] <= tau) lo = mid; else hi = mid;
   }
   U.b = lo;
-  const int t = tau - tile_start[lo];
-  const int tiles_b = tile_start[lo + 1] - tile_start[lo];
+  const int t = tau - T.tile_start[lo];
+  const int tiles_b = T.tile_start[lo + 1] - T.tile_start[lo];
   U.q0 = (tiles_b - 1 - t) * p.rows;
-  U.P = __ldg(p.prefix_lens + U.b);
-  const int cu0 = __ldg(p.cu_seqlens_q + U.b);
-  U.E = __ldg(p.cu_seqlens_q + U.b + 1) - cu0;
+  U.P = T.pre[lo];
+  const int cu0 = T.cu0[lo];
+  U.E = T.cu0[lo + 1] - cu0;
   U.q_last = min(U.q0 + p.rows, U.E) - 1;
   U.q_row0 = cu0 + U.q0;
-  U.kv_base = __ldg(p.kv_indptr + U.b);
+  U.kv_base = T.kvb[lo];
   const KvRange r = kv_range(U.P, U.q0, U.q_last, p.window, BN);
   U.kv_lo = r.kv_lo;
   U.n_tiles = r.n_tiles;
@@ -202,7 +214,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
   const uint32_t sBar = smem_u32(bars);
   uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 64);  // [0] tmem base, [1] abort, [2] bad
   int32_t* tile_start = reinterpret_cast<int32_t*>(misc + 4);
-  int32_t* scan = tile_start + (kMaxSeqs + 1);
+  int32_t* seq_cu0 = tile_start + (kMaxSeqs + 1);
+  int32_t* seq_pre = seq_cu0 + (kMaxSeqs + 1);
+  int32_t* seq_kvb = seq_pre + kMaxSeqs;
+  int32_t* scan = seq_kvb + kMaxSeqs;
+  const SeqTab T{tile_start, seq_cu0, seq_pre, seq_kvb};
   volatile uint32_t* abort_flag = misc + 1;
   const unsigned long long tmo = p.timeout_ns;
   const int win = WIN ? p.window : 0;
@@ -211,9 +227,14 @@ __global__ void __launch_bounds__(kThreads, MINB)
 
   // ---------------------------------------------------------------- set-up
   if (tid == 0) {
-    for (int i = 0; i < B::kCount; ++i)
-      mbar_init(sBar + 8u * i,
-                (i == B::kSFree || i == B::kPFull || i == B::kPFull + 1) ? 128u : 1u);
+    for (int i = 0; i < B::kCount; ++i) {
+      uint32_t cnt = 1u;
+      if (i == B::kSFree || i == B::kPFull || i == B::kPFull + 1 || i == B::kEpi) cnt = 128u;
+      // A Q buffer is free once the unit's last QK^T is done (MMA commit) and
+      // its epilogue has finished staging the output through it (one arrival).
+      if (i == B::kQEmpty || i == B::kQEmpty + 1) cnt = 2u;
+      mbar_init(sBar + 8u * i, cnt);
+    }
     misc[1] = 0u;
     misc[2] = 0u;
     fence_barrier_init();
@@ -242,6 +263,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
       bad = true;
     else
       local += (E + p.rows - 1) / p.rows;
+    seq_cu0[b] = c0;
+    seq_pre[b] = P;
+    seq_kvb[b] = k0;
+    if (b == nseq - 1) seq_cu0[nseq] = c1;
   }
   if (bad) misc[2] = 1u;
   // Exclusive scan of the per-thread counts: warp scans, then warp totals.
@@ -289,13 +314,14 @@ __global__ void __launch_bounds__(kThreads, MINB)
   const uint32_t tmem = misc[0];
 
   // ---------------------------------------------------------------- producer
-  // With two Q buffers the next unit's Q tile is requested right after the
-  // current unit's first K/V tile, so its load overlaps the current unit; with
-  // one, after the last K/V tile (its buffer frees when that unit's last
-  // QK^T completes).
+  // Two iterators over the CTA's sequence of key tiles: K runs up to one tile
+  // ahead of V (a K slot frees when its QK^T is done, a V slot only when its
+  // PV is done), and a unit's Q tile is requested just before its first K.
+  // With a single Q buffer the V iterator first finishes the previous unit,
+  // whose epilogue must release that buffer.
   if (warp == 4) {
     if (lane == 0) {
-      uint32_t it = 0, nq = 0, nk[NS], nv[NS];
+      uint32_t nq = 0, nk[NS], nv[NS];
       for (int s = 0; s < NS; ++s) nk[s] = nv[s] = 0u;
       bool ok = true;
       auto issue_q = [&](const Unit& U) -> bool {
@@ -310,41 +336,50 @@ __global__ void __launch_bounds__(kThreads, MINB)
         ++nq;
         return true;
       };
-      int k = 0;
-      int u = unit_of(0);
-      Unit U;
-      if (u < n_units) {
-        U = decode_unit(p, tile_start, u, BN);
-        ok = issue_q(U);
-      }
-      while (ok && u < n_units) {
-        const int u_next = unit_of(k + 1);
-        Unit Un;
-        for (int j = 0; j < U.n_tiles; ++j, ++it) {
-          const uint32_t s = it % NS, ph = (it / NS) & 1u;
-          const int row = U.kv_base + U.kv_lo + j * BN;
+      int kk = 0, jk = 0, uk = unit_of(0);
+      uint32_t itk = 0;
+      Unit Uk;
+      if (uk < n_units) Uk = decode_unit(p, T, uk, BN);
+      int kv = 0, jv = 0, uv = uk;
+      uint32_t itv = 0;
+      Unit Uv = Uk;
+      while (ok && uv < n_units) {
+        bool do_k = (uk < n_units) && itk <= itv + 1u;
+        if (do_k && NQ == 1 && jk == 0 && itv < itk) do_k = false;
+        if (do_k) {
+          if (jk == 0 && !(ok = issue_q(Uk))) break;
+          const uint32_t s = itk % NS, ph = (itk / NS) & 1u;
           if (!(ok = wait_bounded(sBar + 8u * (B::kKEmpty + s), ph ^ 1u, abort_flag, p.status, tmo)))
             break;
           mbar_arrive_expect_tx(sBar + 8u * (B::kKFull + s), kKVBytes);
+          const int row = Uk.kv_base + Uk.kv_lo + jk * BN;
           for (int c = 0; c < NCH; ++c)
             tma_load_3d(sK + s * kKVBytes + c * kKVChunk, &p.tmap_k, sBar + 8u * (B::kKFull + s),
-                        c * 64, U.g, row);
+                        c * 64, Uk.g, row);
           ++nk[s];
+          ++itk;
+          if (++jk == Uk.n_tiles) {
+            jk = 0;
+            uk = unit_of(++kk);
+            if (uk < n_units) Uk = decode_unit(p, T, uk, BN);
+          }
+        } else {
+          const uint32_t s = itv % NS, ph = (itv / NS) & 1u;
           if (!(ok = wait_bounded(sBar + 8u * (B::kVEmpty + s), ph ^ 1u, abort_flag, p.status, tmo)))
             break;
           mbar_arrive_expect_tx(sBar + 8u * (B::kVFull + s), kKVBytes);
+          const int row = Uv.kv_base + Uv.kv_lo + jv * BN;
           for (int c = 0; c < NCH; ++c)
             tma_load_3d(sV + s * kKVBytes + c * kKVChunk, &p.tmap_v, sBar + 8u * (B::kVFull + s),
-                        c * 64, U.g, row);
+                        c * 64, Uv.g, row);
           ++nv[s];
-          if (j == (NQ == 2 ? 0 : U.n_tiles - 1) && u_next < n_units) {
-            Un = decode_unit(p, tile_start, u_next, BN);
-            if (!(ok = issue_q(Un))) break;
+          ++itv;
+          if (++jv == Uv.n_tiles) {
+            jv = 0;
+            uv = unit_of(++kv);
+            if (uv < n_units) Uv = decode_unit(p, T, uv, BN);
           }
         }
-        ++k;
-        u = u_next;
-        U = Un;
       }
       // Let every copy issued land before the CTA can exit.
       for (uint32_t b = 0; b < NQ; ++b) {
@@ -395,10 +430,14 @@ __global__ void __launch_bounds__(kThreads, MINB)
       };
       uint32_t it = 0, uc = 0;
       bool ok = true;
-      for (int k = 0; ok; ++k) {
-        const int u = unit_of(k);
-        if (u >= n_units) break;
-        const Unit U = decode_unit(p, tile_start, u, BN);
+      int u = unit_of(0);
+      Unit Un;
+      if (u < n_units) Un = decode_unit(p, T, u, BN);
+      for (int k = 0; ok && u < n_units; ++k) {
+        const Unit U = Un;  // decoded one unit ahead: its loads overlap this unit
+        const int u_next = unit_of(k + 1);
+        if (u_next < n_units) Un = decode_unit(p, T, u_next, BN);
+        u = u_next;
         const uint32_t qb = uc % NQ;
         if (!(ok = wait_bounded(sBar + 8u * (B::kQFull + qb), (uc / NQ) & 1u, abort_flag, p.status,
                                 tmo)))
@@ -438,10 +477,28 @@ __global__ void __launch_bounds__(kThreads, MINB)
     const float sl2 = p.scale_log2;
     uint32_t it = 0;
     bool ok = true;
-    for (int k = 0; ok; ++k) {
-      const int u = unit_of(k);
-      if (u >= n_units) break;
-      const Unit U = decode_unit(p, tile_start, u, BN);
+    bool release_pending = false;  // Q buffer to hand back after the next P store
+    uint32_t release_qb = 0;
+    uint32_t n_full = 0;  // units whose output went through the TMA store
+    int u = unit_of(0);
+    Unit Un;
+    float sink_next = 0.f;
+    if (u < n_units) {
+      Un = decode_unit(p, T, u, BN);
+      if (p.sinks != nullptr) sink_next = __ldg(p.sinks + Un.g * p.G + r % p.G);
+    }
+    for (int k = 0; ok && u < n_units; ++k) {
+      // Unit metadata and the sink are fetched one unit ahead, so their
+      // global-memory latency overlaps the previous unit.
+      const Unit U = Un;
+      const int cur_u = u;
+      const float sink = sink_next;
+      const uint32_t qb = (uint32_t)k % NQ;  // this unit's Q buffer
+      u = unit_of(k + 1);
+      if (u < n_units) {
+        Un = decode_unit(p, T, u, BN);
+        if (p.sinks != nullptr) sink_next = __ldg(p.sinks + Un.g * p.G + r % p.G);
+      }
       const int pl = U.q0 + r / p.G;  // query position inside the sequence
       const int h = U.g * p.G + r % p.G;
       const int pos = U.P + pl;
@@ -457,8 +514,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
         // The S row is processed in 64-column chunks so that only one chunk
         // of fp32 scores is live in registers; the packed 16-bit P of earlier
         // chunks (half the size) waits in registers until the tile is done.
-        const bool edge = tile_needs_mask(n0, BN, U.P, U.q0, U.q_last, win);
-        n_masked += edge ? 1 : 0;
+        // Edge tests are uniform over the CTA: the causal edge (a key past the
+        // first row's position) and the window edge (a key below the last
+        // row's lower bound); their union is tile_needs_mask().
+        const bool edge_c = n0 + BN - 1 > U.P + U.q0;
+        const bool edge_w = WIN && n0 < U.P + U.q_last - win + 1;
+        n_masked += (edge_c || edge_w) ? 1 : 0;
         uint32_t pk[BN / 2];
         float alpha = 1.f;  // product of this tile's reference moves
         bool upd_any = false;
@@ -472,14 +533,26 @@ __global__ void __launch_bounds__(kThreads, MINB)
             tc_fence_before();
             mbar_arrive(sBar + 8u * B::kSFree);  // S is in registers: next QK^T may overwrite it
           }
-          // Per-element mask, edge tiles only (uniform over the CTA): row
-          // `pos` keeps columns [c_lo, c_hi] of this chunk.
-          if (edge) {
-            const int c_hi = pos - (n0 + ch * 64);
-            const int c_lo = WIN ? pos - win + 1 - (n0 + ch * 64) : -1;
+          // Per-element mask on edge tiles only: row `pos` keeps columns
+          // [c_lo, c_hi] of this chunk; one-sided tiles test one bound.
+          const int c_hi = pos - (n0 + ch * 64);
+          const int c_lo = pos - win + 1 - (n0 + ch * 64);
+          if (edge_c && edge_w) {
 #pragma unroll
             for (int c = 0; c < 64; ++c)
               if (c > c_hi || c < c_lo) sr[c] = __float_as_uint(-INFINITY);
+          } else if (edge_c) {
+            if (c_hi < 63) {
+#pragma unroll
+              for (int c = 0; c < 64; ++c)
+                if (c > c_hi) sr[c] = __float_as_uint(-INFINITY);
+            }
+          } else if (edge_w) {
+            if (c_lo > 0) {
+#pragma unroll
+              for (int c = 0; c < 64; ++c)
+                if (c < c_lo) sr[c] = __float_as_uint(-INFINITY);
+            }
           }
           // Chunk max over independent chains (short dependency chains).
           float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
@@ -566,6 +639,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(sBar + 8u * (B::kPFull + pb));
+        if (release_pending && r == 0) {
+          // The previous unit's output store has read its staging buffer by now
+          // (or shortly); hand that Q buffer back to the producer.
+          bulk_wait_group_read0();
+          mbar_arrive(sBar + 8u * (B::kQEmpty + release_qb));
+          release_pending = false;
+        }
       }
       if (!ok) break;
 
@@ -575,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
       if (!ok) break;
       tc_fence_after();
       const bool has_x = (p.sinks != nullptr) || (p.smooth != 0);
-      const float ms = (p.sinks != nullptr) ? __ldg(p.sinks + h) * kLog2e : 0.f;
+      const float ms = sink * kLog2e;  // 0 in smooth mode
       float inv = 0.f, lse2 = -INFINITY;
       if (m != -INFINITY) {
         // Same value as l + exp2(ms - m) over the m-referenced sums, computed
@@ -589,6 +669,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
       }
       const bool valid = pl <= U.q_last;
       const size_t orow = (size_t)(U.q_row0 + r / p.G) * p.Hq + h;
+      // A unit whose rows all belong to its sequence is staged in its own Q
+      // buffer (its last QK^T is done) in the 128-byte-swizzled layout of the
+      // output tensor map and written by one TMA store; a ragged tail unit
+      // stores its valid rows directly.
+      const bool full = (U.q_last - U.q0 + 1) == p.rows;
+      const uint32_t stage = sQ + qb * kQBytes;
       uint16_t* op = reinterpret_cast<uint16_t*>(p.out) + orow * D;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {  // 64 columns per round trip
@@ -596,20 +682,51 @@ __global__ void __launch_bounds__(kThreads, MINB)
         tmem_ld32(t_lane + kColO + c * 64, *reinterpret_cast<uint32_t(*)[32]>(o));
         tmem_ld32(t_lane + kColO + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
         tmem_wait_ld();
-        if (valid) {
-          uint32_t w[32];
+        uint32_t w[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+        for (int i = 0; i < 32; ++i)
+          w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+        if (full) {
+          const uint32_t row_addr = stage + c * kQChunk + (uint32_t)r * 128u;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            st_shared_v4(row_addr + ((uint32_t)(i ^ (r & 7)) << 4), w[4 * i], w[4 * i + 1],
+                         w[4 * i + 2], w[4 * i + 3]);
+        } else if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(op + c * 64);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
       }
+      if (full) {
+        fence_proxy_async_smem();  // generic-proxy writes -> visible to the TMA store
+        mbar_arrive(sBar + 8u * B::kEpi);
+        if (r == 0) {
+          if (!wait_bounded(sBar + 8u * B::kEpi, n_full & 1u, abort_flag, p.status, tmo)) {
+            ok = false;
+          } else {
+            for (int c = 0; c < NCH; ++c)
+              tma_store_3d(&p.tmap_o, stage + c * kQChunk, c * 64, U.g * p.G, U.q_row0);
+            bulk_commit_group();
+          }
+        }
+        ++n_full;
+      }
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
       if (valid && p.lse != nullptr) p.lse[orow] = lse2 * kLn2;
+      if (r == 0) {
+        if (NQ == 1) {
+          bulk_wait_group_read0();
+          mbar_arrive(sBar + 8u * (B::kQEmpty + qb));
+        } else {
+          release_pending = true;
+          release_qb = qb;
+        }
+      }
       if (p.unit_log != nullptr && r == 0) {
-        int32_t* rec = p.unit_log + 8 * (size_t)u;
+        int32_t* rec = p.unit_log + 8 * (size_t)cur_u;
         rec[0] = U.b;
         rec[1] = U.g;
         rec[2] = U.q0;
@@ -619,6 +736,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
         rec[6] = (int)blockIdx.x;
         rec[7] = k;
       }
+    }
+    if (r == 0) {
+      bulk_wait_group0();  // every output store complete before the CTA exits
+      if (release_pending) mbar_arrive(sBar + 8u * (B::kQEmpty + release_qb));
     }
   }
 

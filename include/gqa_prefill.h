@@ -88,7 +88,8 @@ enum {
 
 /*
  * gqa_flash_prefill -- the fused prefill (see the definition above).
- *   num_seqs     B >= 0
+ *   num_seqs     B >= 0 (at most 512 per call: the kernel keeps every
+ *                sequence's metadata in shared memory; more is declined)
  *   total_q      rows of q/out (>= cu_seqlens_q[B]); 0 means no work
  *   total_kv     rows of k/v (>= kv_indptr[B])
  *   max_seqlen_q optional host hint, max_b E_b (0 = unknown); only used to
