@@ -286,6 +286,96 @@ def run_ours(args, rank, world):
     return line
 
 
+def run_workload(args, rank, world):
+    """Supplementary workloads: one step = every call of the workload, timed as
+    a whole with CUDA events (L2 flushed before each step, outside the
+    events)."""
+    import torch
+    import gqa_flash_attention_prefill_gb300 as pkg
+    from gqa_flash_attention_prefill_gb300 import workloads as W
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    pkg.load()
+    dev = "cuda"
+    if args.workload == "chunked_prefix":
+        full = W.chunked_prefix(8, 8192, 8192, 128, seed=2)
+        b = W.window_bounded(full, 128) if args.layout == "window-bounded" else full
+        calls = [b.to(dev)]
+        desc = (f"chunked prefill over cached prefix: B=8, prefix 8192 + extend 8192, 64/8, d 64, "
+                f"bf16, window 128, sinks, {args.layout} KV layout")
+        tokens = 8 * 8192
+    elif args.workload == "oss20b_16k":
+        grid = W.oss20b_prefill(num_layers=24, seq=16384, chunk_len=512, seed=3, device=dev)
+        calls = [c for row in grid for c in row]  # chunk-major: the prefill's order
+        desc = ("gpt-oss-20b-like 16k prefill: 24 layers (12 full, 12 window-128), 64/8, d 64, "
+                "bf16, 32 chunks of 512 over a growing prefix, sinks (768 calls per step)")
+        tokens = 16384
+    elif args.workload == "ragged":
+        b = W.ragged(hq=64, hkv=8, d=64, dtype="bf16", window=128, sink_mode="head", seed=4)
+        calls = [b.to(dev)]
+        desc = ("ragged varlen: 16 sequences, prefixes U[0,16384], extends U[1,8192], 64/8, d 64, "
+                "bf16, window 128, sinks")
+        tokens = b.total_q
+    else:
+        raise ValueError(args.workload)
+    flops = 0.0
+    for b in calls:
+        flops += 4.0 * b.d * b.hq * useful_pairs([int(x) for x in b.prefix_lens.tolist()],
+                                                 b.extend_lens, b.window)
+    outs = [torch.empty_like(b.q) for b in calls]
+    lses = [torch.empty(b.q.shape[:2], dtype=torch.float32, device=dev) for b in calls]
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        for b, o, l in zip(calls, outs, lses):
+            pkg.prefill(b, out=o, lse=l, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if pkg.get_device_status() != 0:
+        raise RuntimeError("device status word raised during warm-up")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    dist_barrier(world)
+    ms_step = dist_max(statistics.mean(e[0].elapsed_time(e[1]) for e in ev), world)
+    peaks = load_peaks()
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) Q/K/V and sinks; no model weights)",
+            "config": {"workload": desc, "l2": "flushed between steps (256 MiB write)",
+                       "calls_per_step": len(calls)},
+            "tokens_per_s": round(world * tokens / (ms_step * 1e-3), 1),
+            "pct_of_bf16_peak": round(100.0 * value / (world * peaks["bf16_tflops"]), 2),
+            "gpu_launches": len(calls) * args.steps, "clocks": clk.summary()}
+    if args.workload == "chunked_prefix":
+        # HBM-bound: Q read and O (+ lse) written once; of K and V only the rows some
+        # window reaches (the window-bounded layout's rows) must be read, in either layout.
+        nbytes = 0
+        for b in calls:
+            keys = sum(min(p_, b.window) + e for p_, e in
+                       zip([int(x) for x in b.prefix_lens.tolist()], b.extend_lens))
+            nbytes += b.q.numel() * 2 * 2 + keys * b.hkv * b.d * 2 * 2 + b.q.shape[0] * b.hq * 4
+        gbs = nbytes / (ms_step * 1e-3) / 1e9
+        line["roofline"] = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                            "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                            "traffic": None, "algorithmic_bytes": nbytes}
+    return line
+
+
 def oracle_sample_run(layers_cpu, rows_per_layer, offset=0):
     """Runs the CPU oracle on `rows_per_layer` evenly spaced query rows of
     each layer; returns (seconds, useful flops, rows)."""
@@ -374,12 +464,20 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="CPU work of the oracle baseline sample (rank 0, N=1)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="layer_pair",
+                    choices=["layer_pair", "chunked_prefix", "oss20b_16k", "ragged"],
+                    help="layer_pair is the headline configuration; the others are "
+                         "supplementary measurements")
+    ap.add_argument("--layout", default="window-bounded", choices=["window-bounded", "full-prefix"],
+                    help="KV layout of the chunked_prefix workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world = dist_setup()
     if args.impl == "reference":
         line = run_reference(args, rank, world)
+    elif args.workload != "layer_pair":
+        line = run_workload(args, rank, world)
     else:
         line = run_ours(args, rank, world)
         if rank == 0:

@@ -13,7 +13,8 @@ import os
 from typing import Optional
 
 __all__ = ["load", "gqa_flash_prefill", "gqa_flash_prefill_debug", "prefill",
-           "plan", "force_block_n", "get_device_status", "GQAError",
+           "plan", "force_block_n", "get_device_status", "set_tuning",
+           "clear_config_cache", "config_block_n", "selftest_timeout", "GQAError",
            "GQA_F16", "GQA_BF16", "GQA_DEV_TIMEOUT", "GQA_DEV_BAD_METADATA",
            "EXPORTED_SYMBOLS"]
 
@@ -24,7 +25,9 @@ GQA_DEV_TIMEOUT, GQA_DEV_BAD_METADATA = 1, 2
 EXPORTED_SYMBOLS = [
     "gqa_flash_prefill", "gqa_flash_prefill_debug", "gqa_prefill_plan",
     "gqa_prefill_force_block_n", "gqa_prefill_get_device_status",
-    "gqa_prefill_status_string", "gqa_prefill_version",
+    "gqa_prefill_status_string", "gqa_prefill_version", "gqa_prefill_set_tuning",
+    "gqa_prefill_clear_config_cache", "gqa_prefill_config_block_n",
+    "gqa_prefill_selftest_timeout",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -74,6 +77,16 @@ def load(path: Optional[str] = None):
     lib.gqa_prefill_status_string.restype = ctypes.c_char_p
     lib.gqa_prefill_version.argtypes = []
     lib.gqa_prefill_version.restype = ctypes.c_char_p
+    lib.gqa_prefill_set_tuning.argtypes = [ctypes.c_int]
+    lib.gqa_prefill_set_tuning.restype = ctypes.c_int
+    lib.gqa_prefill_clear_config_cache.argtypes = []
+    lib.gqa_prefill_clear_config_cache.restype = ctypes.c_int
+    lib.gqa_prefill_config_block_n.argtypes = [ctypes.c_int] * 7 + [
+        ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
+    lib.gqa_prefill_config_block_n.restype = ctypes.c_int
+    lib.gqa_prefill_selftest_timeout.argtypes = [ctypes.c_int, ctypes.c_void_p,
+                                                 ctypes.POINTER(ctypes.c_int)]
+    lib.gqa_prefill_selftest_timeout.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib
@@ -185,6 +198,39 @@ def force_block_n(block_n: int) -> None:
     rc = load().gqa_prefill_force_block_n(int(block_n))
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_prefill_force_block_n")
+
+
+def set_tuning(enable: bool) -> None:
+    """Turn the configuration cache's timed sweep on or off (see gqa_prefill.h)."""
+    rc = load().gqa_prefill_set_tuning(1 if enable else 0)
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_prefill_set_tuning")
+
+
+def clear_config_cache() -> None:
+    load().gqa_prefill_clear_config_cache()
+
+
+def config_block_n(total_q, max_seqlen_q, hq, hkv, d, dtype, window):
+    """(block_n, tuned) cached for these shapes; block_n 0 = no entry yet."""
+    bn, tuned = ctypes.c_int(0), ctypes.c_int(0)
+    code = dtype if isinstance(dtype, int) else (GQA_BF16 if "bf16" in str(dtype) else GQA_F16)
+    rc = load().gqa_prefill_config_block_n(int(total_q), int(max_seqlen_q), int(hq), int(hkv),
+                                           int(d), code, int(window), ctypes.byref(bn),
+                                           ctypes.byref(tuned))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_prefill_config_block_n")
+    return bn.value, bool(tuned.value)
+
+
+def selftest_timeout(timeout_ms: int = 50, stream=None) -> int:
+    """Run the bounded-wait self-test; returns the device status word it read."""
+    st = ctypes.c_int(0)
+    rc = load().gqa_prefill_selftest_timeout(int(timeout_ms), _stream_handle(stream),
+                                             ctypes.byref(st))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_prefill_selftest_timeout")
+    return st.value
 
 
 def get_device_status() -> int:

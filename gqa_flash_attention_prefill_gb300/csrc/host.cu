@@ -20,6 +20,21 @@ namespace gqa {
 // Device status word (GQA_DEV_* bits); kernels receive its address.
 __device__ unsigned int g_device_status;
 
+// Failure-detection self-test: one thread waits on an mbarrier that nothing
+// ever arrives on, through the same bounded wait the prefill kernel uses.  The
+// wait runs out after `timeout_ns`, raises GQA_DEV_TIMEOUT and the kernel
+// returns normally, so the context stays usable.
+__global__ void selftest_wait_kernel(unsigned int* status, unsigned long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0u;
+    mbar_init(smem_u32(&bar), 1u);
+    fence_barrier_init();
+    (void)wait_bounded(smem_u32(&bar), 0u, &abort_flag, status, timeout_ns);
+  }
+}
+
 namespace {
 
 std::mutex g_mu;      // guards the configuration cache and the forced tile size
@@ -40,7 +55,12 @@ std::map<int, DeviceInfo> g_devices;
 // commit), while a window caps the tiles walked and so may change the winner
 // (same page, window commit).
 using CfgKey = std::tuple<int, int, int, int, int, int>;
-std::map<CfgKey, int> g_cfg_cache;
+struct CfgEntry {
+  int block_n;
+  bool tuned;  // chosen by a timed sweep rather than the default
+};
+std::map<CfgKey, CfgEntry> g_cfg_cache;
+int g_tune_mode = -1;  // -1: read GQA_PREFILL_TUNE on first use; 0 off; 1 on
 
 bool env_flag(const char* name) {
   const char* v = std::getenv(name);
@@ -108,8 +128,22 @@ struct Plan {
   unsigned smem_launch;  // dynamic smem requested per CTA
 };
 
+CfgKey cfg_key(int d, int total_q, int max_seqlen_q, int Hq, int G, int window, int dtype) {
+  return CfgKey{d, pow2_bucket(max_seqlen_q > 0 ? max_seqlen_q : total_q), Hq, G,
+                window > 0 ? 1 : 0, dtype};
+}
+
+// Plan for an explicit tile size (block_n > 0) or the cache's choice (0).
+int make_plan_bn(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, int d, int dtype,
+                 int window, int force_bn, Plan* pl);
+
 int make_plan(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, int d, int dtype,
               int window, Plan* pl) {
+  return make_plan_bn(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, 0, pl);
+}
+
+int make_plan_bn(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, int d, int dtype,
+                 int window, int force_bn, Plan* pl) {
   if (num_seqs < 0 || total_q < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0)
     return GQA_ERR_INVALID;
   if (dtype != GQA_F16 && dtype != GQA_BF16) return GQA_ERR_INVALID;
@@ -119,18 +153,17 @@ int make_plan(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, int 
   if (num_seqs > kMaxSeqs) return GQA_ERR_UNSUPPORTED;
   DeviceInfo di;
   const bool have_dev = device_info(&di) == GQA_OK;
-  int bn;
-  {
+  int bn = force_bn;
+  if (bn == 0) {
     std::lock_guard<std::mutex> lk(g_mu);
     if (g_forced_block_n != 0) {
       bn = g_forced_block_n;
     } else {
-      const CfgKey key{d, pow2_bucket(max_seqlen_q > 0 ? max_seqlen_q : total_q), Hq, G,
-                       window > 0 ? 1 : 0, dtype};
+      const CfgKey key = cfg_key(d, total_q, max_seqlen_q, Hq, G, window, dtype);
       auto itr = g_cfg_cache.find(key);
       if (itr == g_cfg_cache.end())
-        itr = g_cfg_cache.emplace(key, default_block_n(d, window > 0)).first;
-      bn = itr->second;
+        itr = g_cfg_cache.emplace(key, CfgEntry{default_block_n(d, window > 0), false}).first;
+      bn = itr->second.block_n;
     }
   }
   if (!kernel_shape(d, bn, &pl->shape)) return GQA_ERR_UNSUPPORTED;
@@ -180,31 +213,18 @@ int encode_map(CUtensorMap* m, const void* base, int dtype, int d, int heads, in
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int run(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
-        const int32_t* prefix_lens, const int32_t* kv_indptr, int num_seqs, int total_q,
-        int total_kv, int max_seqlen_q, int Hq, int Hkv, int d, int dtype, float scale,
-        int window, const float* sinks, int smooth_softmax, void* out, float* lse, void* stream,
-        int32_t* unit_log) {
-  if (num_seqs < 0 || total_q < 0 || total_kv < 0 || max_seqlen_q < 0) return GQA_ERR_INVALID;
-  if (Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return GQA_ERR_INVALID;
-  if (dtype != GQA_F16 && dtype != GQA_BF16) return GQA_ERR_INVALID;
-  if (!(scale > 0.f) || !std::isfinite(scale)) return GQA_ERR_INVALID;
-  if (sinks != nullptr && smooth_softmax != 0) return GQA_ERR_INVALID;
-  if (num_seqs == 0 || total_q == 0) return GQA_OK;  // no work, no launch
-  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr ||
-      cu_seqlens_q == nullptr || prefix_lens == nullptr || kv_indptr == nullptr)
-    return GQA_ERR_INVALID;
-  if (total_kv == 0) return GQA_ERR_INVALID;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return GQA_ERR_INVALID;
-  Plan pl;
-  int rc = make_plan(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, &pl);
-  if (rc != GQA_OK) return rc;
+// Encodes the tensor maps and launches one planned kernel on `stream`.
+int launch_planned(const Plan& pl, const void* q, const void* k, const void* v,
+                   const int32_t* cu_seqlens_q, const int32_t* prefix_lens,
+                   const int32_t* kv_indptr, int num_seqs, int total_q, int total_kv, int Hq,
+                   int Hkv, int d, int dtype, float scale, int window, const float* sinks,
+                   int smooth_softmax, void* out, float* lse, void* stream, int32_t* unit_log) {
   DeviceInfo di;
   if (device_info(&di) != GQA_OK) return GQA_ERR_CUDA;
 
   PrefillParams p;
   std::memset(&p, 0, sizeof(p));
-  rc = encode_map(&p.tmap_q, q, dtype, d, Hq, total_q, pl.G, pl.rows);
+  int rc = encode_map(&p.tmap_q, q, dtype, d, Hq, total_q, pl.G, pl.rows);
   if (rc == GQA_OK) rc = encode_map(&p.tmap_k, k, dtype, d, Hkv, total_kv, 1, pl.shape.block_n);
   if (rc == GQA_OK) rc = encode_map(&p.tmap_v, v, dtype, d, Hkv, total_kv, 1, pl.shape.block_n);
   if (rc == GQA_OK) rc = encode_map(&p.tmap_o, out, dtype, d, Hq, total_q, pl.G, pl.rows);
@@ -251,6 +271,117 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q
                  pl.shape.kv_stages, pl.grid, pl.ctas_per_sm, pl.max_units,
                  e == cudaSuccess ? "launched" : cudaGetErrorString(e));
   return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+int tune_mode() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_tune_mode < 0) g_tune_mode = env_flag("GQA_PREFILL_TUNE") ? 1 : 0;
+  return g_tune_mode;
+}
+
+// The configuration cache's sweep ([HIPEP] config-cache commit: one sweep per
+// key and process; tuning launches omit the sink, which cannot reorder the
+// candidates): times every candidate tile size on the caller's stream and
+// keeps the fastest.  Synchronises the stream; skipped while capturing.
+int tune_key(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+             const int32_t* prefix_lens, const int32_t* kv_indptr, int num_seqs, int total_q,
+             int total_kv, int max_seqlen_q, int Hq, int Hkv, int d, int dtype, float scale,
+             int window, void* out, float* lse, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+    return GQA_OK;
+  const int cands[2] = {64, 128};
+  int best = 0;
+  float best_ms = 0.f;
+  cudaEvent_t e0, e1;
+  if (cudaEventCreate(&e0) != cudaSuccess) return GQA_ERR_CUDA;
+  if (cudaEventCreate(&e1) != cudaSuccess) {
+    cudaEventDestroy(e0);
+    return GQA_ERR_CUDA;
+  }
+  int rc = GQA_OK;
+  for (int bn : cands) {
+    Plan pl;
+    KernelShape ks;
+    if (!kernel_shape(d, bn, &ks)) continue;
+    rc = make_plan_bn(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, bn, &pl);
+    if (rc != GQA_OK) break;
+    auto once = [&]() {
+      return launch_planned(pl, q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs, total_q,
+                            total_kv, Hq, Hkv, d, dtype, scale, window, nullptr, 0, out, lse,
+                            stream, nullptr);
+    };
+    if ((rc = once()) != GQA_OK) break;
+    cudaEventRecord(e0, st);
+    for (int i = 0; i < 3 && rc == GQA_OK; ++i) rc = once();
+    cudaEventRecord(e1, st);
+    if (rc != GQA_OK || cudaEventSynchronize(e1) != cudaSuccess) {
+      rc = rc != GQA_OK ? rc : GQA_ERR_CUDA;
+      break;
+    }
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, e0, e1);
+    ms /= 3.f;
+    if (env_flag("GQA_PREFILL_TUNE_DEBUG"))
+      std::fprintf(stderr, "[gqa_prefill tune] d=%d sq<=%d Hq=%d G=%d windowed=%d block_n=%d: %.4f ms\n",
+                   d, pow2_bucket(max_seqlen_q > 0 ? max_seqlen_q : total_q), Hq, Hq / Hkv,
+                   window > 0 ? 1 : 0, bn, ms);
+    if (best == 0 || ms < best_ms) {
+      best = bn;
+      best_ms = ms;
+    }
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (rc != GQA_OK) return rc;
+  if (best != 0) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_cfg_cache[cfg_key(d, total_q, max_seqlen_q, Hq, Hq / Hkv, window, dtype)] =
+        CfgEntry{best, true};
+  }
+  return GQA_OK;
+}
+
+int run(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+        const int32_t* prefix_lens, const int32_t* kv_indptr, int num_seqs, int total_q,
+        int total_kv, int max_seqlen_q, int Hq, int Hkv, int d, int dtype, float scale,
+        int window, const float* sinks, int smooth_softmax, void* out, float* lse, void* stream,
+        int32_t* unit_log) {
+  if (num_seqs < 0 || total_q < 0 || total_kv < 0 || max_seqlen_q < 0) return GQA_ERR_INVALID;
+  if (Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return GQA_ERR_INVALID;
+  if (dtype != GQA_F16 && dtype != GQA_BF16) return GQA_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return GQA_ERR_INVALID;
+  if (sinks != nullptr && smooth_softmax != 0) return GQA_ERR_INVALID;
+  if (num_seqs == 0 || total_q == 0) return GQA_OK;  // no work, no launch
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr ||
+      cu_seqlens_q == nullptr || prefix_lens == nullptr || kv_indptr == nullptr)
+    return GQA_ERR_INVALID;
+  if (total_kv == 0) return GQA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return GQA_ERR_INVALID;
+  if (d != 64 && d != 128 && d != 256) return GQA_ERR_UNSUPPORTED;
+  if (tune_mode() == 1) {
+    bool need = false;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      if (g_forced_block_n == 0) {
+        auto itr = g_cfg_cache.find(cfg_key(d, total_q, max_seqlen_q, Hq, Hq / Hkv, window, dtype));
+        need = itr == g_cfg_cache.end() || !itr->second.tuned;
+      }
+    }
+    if (need) {
+      const int rc = tune_key(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs, total_q,
+                              total_kv, max_seqlen_q, Hq, Hkv, d, dtype, scale, window, out, lse,
+                              stream);
+      if (rc != GQA_OK) return rc;
+    }
+  }
+  Plan pl;
+  const int rc = make_plan(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, &pl);
+  if (rc != GQA_OK) return rc;
+  return launch_planned(pl, q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs, total_q,
+                        total_kv, Hq, Hkv, d, dtype, scale, window, sinks, smooth_softmax, out, lse,
+                        stream, unit_log);
 }
 
 }  // namespace
@@ -310,6 +441,48 @@ int gqa_prefill_plan(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hk
   plan->grid = pl.grid;
   plan->max_units = pl.max_units;
   return GQA_OK;
+}
+
+int gqa_prefill_set_tuning(int enable) {
+  if (enable != 0 && enable != 1) return GQA_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(gqa::g_mu);
+  gqa::g_tune_mode = enable;
+  return GQA_OK;
+}
+
+int gqa_prefill_clear_config_cache(void) {
+  std::lock_guard<std::mutex> lk(gqa::g_mu);
+  gqa::g_cfg_cache.clear();
+  return GQA_OK;
+}
+
+int gqa_prefill_config_block_n(int total_q, int max_seqlen_q, int Hq, int Hkv, int d, int dtype,
+                               int window, int* block_n, int* tuned) {
+  if (block_n == nullptr || tuned == nullptr || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
+    return GQA_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(gqa::g_mu);
+  auto itr = gqa::g_cfg_cache.find(
+      gqa::cfg_key(d, total_q, max_seqlen_q, Hq, Hq / Hkv, window, dtype));
+  if (itr == gqa::g_cfg_cache.end()) {
+    *block_n = 0;
+    *tuned = 0;
+  } else {
+    *block_n = itr->second.block_n;
+    *tuned = itr->second.tuned ? 1 : 0;
+  }
+  return GQA_OK;
+}
+
+int gqa_prefill_selftest_timeout(int timeout_ms, void* stream, int* status) {
+  if (status == nullptr || timeout_ms <= 0 || timeout_ms > 10000) return GQA_ERR_INVALID;
+  gqa::DeviceInfo di;
+  if (gqa::device_info(&di) != GQA_OK) return GQA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  gqa::selftest_wait_kernel<<<1, 32, 0, st>>>(di.status,
+                                              (unsigned long long)timeout_ms * 1000000ull);
+  if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return GQA_ERR_CUDA;
+  return gqa_prefill_get_device_status(status);
 }
 
 int gqa_prefill_force_block_n(int block_n) {

@@ -81,18 +81,18 @@ class Batch:
                      self.name, dict(self.meta))
 
 
-def _normal(gen, shape, dtype):
-    return torch.randn(*shape, generator=gen, dtype=torch.float32).to(dtype)
+def _normal(gen, shape, dtype, device="cpu"):
+    return torch.randn(*shape, generator=gen, dtype=torch.float32, device=device).to(dtype)
 
 
 def make_batch(prefix_lens, extend_lens, hq, hkv, d, dtype="bf16", window=0,
-               sink_mode="head", seed=0, scale=None, name="") -> Batch:
+               sink_mode="head", seed=0, scale=None, name="", device="cpu") -> Batch:
     """Ragged batch: sequence b has prefix_lens[b] cached keys followed by
     extend_lens[b] new tokens; its KV rows are packed [prefix | extend] back to
     back in sequence order.  sink_mode is "none", "head" or "smooth"."""
     assert len(prefix_lens) == len(extend_lens)
     dt = DTYPES[dtype] if isinstance(dtype, str) else dtype
-    gen = torch.Generator().manual_seed(int(seed))
+    gen = torch.Generator(device=device).manual_seed(int(seed))
     b = len(prefix_lens)
     cu = [0]
     kvp = [0]
@@ -100,18 +100,18 @@ def make_batch(prefix_lens, extend_lens, hq, hkv, d, dtype="bf16", window=0,
         cu.append(cu[-1] + int(e))
         kvp.append(kvp[-1] + int(p) + int(e))
     total_q, total_kv = cu[-1], kvp[-1]
-    q = _normal(gen, (total_q, hq, d), dt)
-    k = _normal(gen, (total_kv, hkv, d), dt)
-    v = _normal(gen, (total_kv, hkv, d), dt)
+    q = _normal(gen, (total_q, hq, d), dt, device)
+    k = _normal(gen, (total_kv, hkv, d), dt, device)
+    v = _normal(gen, (total_kv, hkv, d), dt, device)
     sinks = None
     if sink_mode == "head":
-        sinks = _normal(gen, (hq,), dt).to(torch.float32)
+        sinks = _normal(gen, (hq,), dt, device).to(torch.float32)
     elif sink_mode not in ("none", "smooth"):
         raise ValueError(sink_mode)
     return Batch(q, k, v,
-                 torch.tensor(cu, dtype=torch.int32),
-                 torch.tensor([int(p) for p in prefix_lens], dtype=torch.int32),
-                 torch.tensor(kvp, dtype=torch.int32),
+                 torch.tensor(cu, dtype=torch.int32, device=device),
+                 torch.tensor([int(p) for p in prefix_lens], dtype=torch.int32, device=device),
+                 torch.tensor(kvp, dtype=torch.int32, device=device),
                  hq, hkv, d, int(window), sinks, sink_mode == "smooth",
                  float(scale if scale is not None else d ** -0.5), name,
                  {"seed": int(seed), "num_seqs": b})
@@ -179,6 +179,36 @@ def oss20b_chunk(layer: int, chunk: int, chunk_len: int = 512,
                       window=window, sink_mode="head",
                       seed=seed * 100003 + layer * 1009 + chunk,
                       name=f"oss20b-L{layer}-c{chunk}")
+
+
+def oss20b_prefill(num_layers: int = 24, seq: int = 16384, chunk_len: int = 512,
+                   seed: int = 3, device="cpu") -> List[List[Batch]]:
+    """The calls of a gpt-oss-20b-like prefill of `seq` tokens in chunks of
+    `chunk_len`: calls[c][layer] for chunk c and layer, layers alternating
+    full-causal (even) and window-128 (odd).  Each layer has one KV cache of
+    `seq` tokens and one query tensor; chunk c is a view of query rows
+    [c*chunk_len, (c+1)*chunk_len) over the first (c+1)*chunk_len keys."""
+    n_chunks = seq // chunk_len
+    layers = []
+    for layer in range(num_layers):
+        full = make_batch([0], [seq], 64, 8, 64, "bf16", window=0 if layer % 2 == 0 else 128,
+                          sink_mode="head", seed=seed * 100003 + layer, device=device,
+                          name=f"oss20b-L{layer}")
+        layers.append(full)
+    calls = []
+    for c in range(n_chunks):
+        row = []
+        for layer, t in enumerate(layers):
+            lo, hi = c * chunk_len, (c + 1) * chunk_len
+            row.append(Batch(t.q[lo:hi], t.k[:hi], t.v[:hi],
+                             torch.tensor([0, chunk_len], dtype=torch.int32, device=device),
+                             torch.tensor([lo], dtype=torch.int32, device=device),
+                             torch.tensor([0, hi], dtype=torch.int32, device=device),
+                             64, 8, 64, t.window, t.sinks, False, t.scale,
+                             f"oss20b-L{layer}-c{c}", {"max_seqlen_q": chunk_len,
+                                                       "extend_lens": [chunk_len]}))
+        calls.append(row)
+    return calls
 
 
 RAGGED_WINDOWS = [1, 15, 64, 127, 128, 129, 4096, 0]

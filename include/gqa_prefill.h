@@ -156,6 +156,39 @@ int gqa_flash_prefill_debug(const void* q, const void* k, const void* v,
 int gqa_prefill_force_block_n(int block_n);
 
 /*
+ * Launch-configuration tuning.  The configuration cache is keyed on (d, a
+ * power-of-two bucket of max_seqlen_q, Hq, G, windowed, dtype), never on the
+ * KV length.  With tuning on (this call, or GQA_PREFILL_TUNE=1 in the
+ * environment before the first call), the first call for an untuned key times
+ * every candidate tile size on the caller's stream (without the sink) and
+ * keeps the fastest; that call synchronises its stream, and tuning is skipped
+ * while the stream is being captured.  GQA_PREFILL_TUNE_DEBUG=1 prints the
+ * timings.  enable: 0 or 1.  Returns GQA_OK or GQA_ERR_INVALID.
+ */
+int gqa_prefill_set_tuning(int enable);
+
+/* Forget every cached configuration (tuned or default).  Returns GQA_OK. */
+int gqa_prefill_clear_config_cache(void);
+
+/*
+ * The cached tile size for a call with these shapes: *block_n = 0 if the key
+ * has no entry yet; *tuned = 1 if the entry came from a timed sweep.
+ */
+int gqa_prefill_config_block_n(int total_q, int max_seqlen_q, int Hq, int Hkv,
+                               int d, int dtype, int window, int* block_n,
+                               int* tuned);
+
+/*
+ * Failure-detection self-test: launches one thread that waits, through the
+ * same bounded wait the prefill kernel uses, on a barrier nothing completes.
+ * The wait gives up after timeout_ms (1..10000), records GQA_DEV_TIMEOUT in
+ * the device status word and returns; the call synchronises `stream`, then
+ * reads and clears the status word into *status (expected GQA_DEV_TIMEOUT).
+ * The CUDA context stays usable afterwards.
+ */
+int gqa_prefill_selftest_timeout(int timeout_ms, void* stream, int* status);
+
+/*
  * Read and clear the device status word of the current device (bits
  * GQA_DEV_*).  Synchronises the device first.  Returns GQA_OK or
  * GQA_ERR_CUDA; *status receives the bits.
