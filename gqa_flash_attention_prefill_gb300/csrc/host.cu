@@ -291,7 +291,7 @@ int tune_key(const void* q, const void* k, const void* v, const int32_t* cu_seql
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(st, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
     return GQA_OK;
-  const int cands[2] = {64, 128};
+  const int cands[3] = {64, 96, 128};
   int best = 0;
   float best_ms = 0.f;
   cudaEvent_t e0, e1;
@@ -391,6 +391,7 @@ bool kernel_shape(int d, int block_n, KernelShape* out) {
   s.block_n = block_n;
   if (d == 64 && block_n == 128) { s.kv_stages = 2; s.min_blocks = 2; }
   else if (d == 64 && block_n == 64) { s.kv_stages = 4; s.min_blocks = 2; }
+  else if (d == 64 && block_n == 96) { s.kv_stages = 2; s.min_blocks = 2; }
   else if (d == 128 && block_n == 64) { s.kv_stages = 2; s.min_blocks = 2; }
   else if (d == 128 && block_n == 128) { s.kv_stages = 2; s.min_blocks = 1; }
   else if (d == 256 && block_n == 64) { s.kv_stages = 2; s.min_blocks = 1; }
@@ -486,7 +487,7 @@ int gqa_prefill_selftest_timeout(int timeout_ms, void* stream, int* status) {
 }
 
 int gqa_prefill_force_block_n(int block_n) {
-  if (block_n != 0 && block_n != 64 && block_n != 128) return GQA_ERR_INVALID;
+  if (block_n != 0 && block_n != 64 && block_n != 96 && block_n != 128) return GQA_ERR_INVALID;
   std::lock_guard<std::mutex> lk(gqa::g_mu);
   gqa::g_forced_block_n = block_n;
   return GQA_OK;

@@ -190,7 +190,7 @@ template <int D, int BN, int NS, bool WIN, bool BF16, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB)
     prefill_kernel(const __grid_constant__ PrefillParams p) {
   static_assert(D == 64 || D == 128 || D == 256, "head dim");
-  static_assert(BN == 64 || BN == 128, "key tile");
+  static_assert(BN == 64 || BN == 96 || BN == 128, "key tile");
   constexpr int NCH = D / 64;  // 128-byte swizzle chunks along d
   constexpr uint32_t kQBytes = 128u * D * 2u;
   constexpr uint32_t kKVBytes = (uint32_t)BN * D * 2u;
@@ -520,44 +520,50 @@ __global__ void __launch_bounds__(kThreads, MINB)
         const bool edge_c = n0 + BN - 1 > U.P + U.q0;
         const bool edge_w = WIN && n0 < U.P + U.q_last - win + 1;
         n_masked += (edge_c || edge_w) ? 1 : 0;
+        // S is processed in CW-column chunks (64, or 48 for 96-key tiles).
+        constexpr int CW = (BN == 96) ? 48 : 64;
+        constexpr int NCK = BN / CW;
         uint32_t pk[BN / 2];
         float alpha = 1.f;  // product of this tile's reference moves
         bool upd_any = false;
 #pragma unroll
-        for (int ch = 0; ch < BN / 64; ++ch) {
+        for (int ch = 0; ch < NCK; ++ch) {
           uint32_t sr[64];
-          tmem_ld32(t_lane + kColS + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(sr));
-          tmem_ld32(t_lane + kColS + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+          tmem_ld32(t_lane + kColS + ch * CW, *reinterpret_cast<uint32_t(*)[32]>(sr));
+          if constexpr (CW == 64)
+            tmem_ld32(t_lane + kColS + ch * CW + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+          else
+            tmem_ld16(t_lane + kColS + ch * CW + 32, *reinterpret_cast<uint32_t(*)[16]>(sr + 32));
           tmem_wait_ld();
-          if (ch == BN / 64 - 1) {
+          if (ch == NCK - 1) {
             tc_fence_before();
             mbar_arrive(sBar + 8u * B::kSFree);  // S is in registers: next QK^T may overwrite it
           }
           // Per-element mask on edge tiles only: row `pos` keeps columns
           // [c_lo, c_hi] of this chunk; one-sided tiles test one bound.
-          const int c_hi = pos - (n0 + ch * 64);
-          const int c_lo = pos - win + 1 - (n0 + ch * 64);
+          const int c_hi = pos - (n0 + ch * CW);
+          const int c_lo = pos - win + 1 - (n0 + ch * CW);
           if (edge_c && edge_w) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c)
+            for (int c = 0; c < CW; ++c)
               if (c > c_hi || c < c_lo) sr[c] = __float_as_uint(-INFINITY);
           } else if (edge_c) {
-            if (c_hi < 63) {
+            if (c_hi < CW - 1) {
 #pragma unroll
-              for (int c = 0; c < 64; ++c)
+              for (int c = 0; c < CW; ++c)
                 if (c > c_hi) sr[c] = __float_as_uint(-INFINITY);
             }
           } else if (edge_w) {
             if (c_lo > 0) {
 #pragma unroll
-              for (int c = 0; c < 64; ++c)
+              for (int c = 0; c < CW; ++c)
                 if (c < c_lo) sr[c] = __float_as_uint(-INFINITY);
             }
           }
           // Chunk max over independent chains (short dependency chains).
           float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < 64; c += 8) {
+          for (int c = 0; c < CW; c += 8) {
             mx0 = max3(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
             mx1 = max3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
             mx2 = max3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
@@ -571,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
             m = m_cand;
             upd_any = true;
 #pragma unroll
-            for (int i = 0; i < ch * 32; ++i) {  // earlier chunks of this tile
+            for (int i = 0; i < ch * (CW / 2); ++i) {  // earlier chunks of this tile
               const float lo = unpack_lo<BF16>(pk[i]) * a, hi = unpack_hi<BF16>(pk[i]) * a;
               pk[i] = pack2<BF16>(lo, hi);
             }
@@ -582,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
           const uint64_t sc2 = f2(sl2, sl2), nm2 = f2(neg_m, neg_m);
           uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;  // packed partial sums
 #pragma unroll
-          for (int c = 0; c < 64; c += 8) {
+          for (int c = 0; c < CW; c += 8) {
             float x[8];
 #pragma unroll
             for (int t = 0; t < 8; t += 2)
@@ -595,7 +601,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
             acc2 = fadd2(acc2, f2(x[4], x[5]));
             acc3 = fadd2(acc3, f2(x[6], x[7]));
 #pragma unroll
-            for (int t = 0; t < 8; t += 2) pk[ch * 32 + (c + t) / 2] = pack2<BF16>(x[t], x[t + 1]);
+            for (int t = 0; t < 8; t += 2)
+              pk[ch * (CW / 2) + (c + t) / 2] = pack2<BF16>(x[t], x[t + 1]);
           }
           float r0, r1;
           unf2(fadd2(fadd2(acc0, acc1), fadd2(acc2, acc3)), r0, r1);
@@ -614,6 +621,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
         for (int c = 0; c < BN / 64; ++c)
           tmem_st32(t_lane + kColP + pb * (BN / 2) + c * 32,
                     *reinterpret_cast<uint32_t(*)[32]>(pk + c * 32));
+        if constexpr (BN == 96)  // the last 16 packed columns
+          tmem_st16(t_lane + kColP + pb * (BN / 2) + 32,
+                    *reinterpret_cast<uint32_t(*)[16]>(pk + 32));
         const bool corr = upd_any && j > 0;
         if (__any_sync(0xffffffffu, corr)) {
           // Rescaling O needs every earlier PV done (PVs complete in order).

@@ -150,8 +150,10 @@ int gqa_flash_prefill_debug(const void* q, const void* k, const void* v,
 
 /*
  * Force the KV tile size for later calls in this process (0 restores the
- * configuration cache's choice).  Valid values: 64 or 128 (d = 256 allows 64
- * only).  Returns GQA_OK or GQA_ERR_INVALID.  Meant for tests and tuning.
+ * configuration cache's choice).  Valid values: 64, 96 or 128; 96 exists for
+ * d = 64 only and d = 256 allows 64 only (a call whose d has no kernel for
+ * the forced size returns GQA_ERR_UNSUPPORTED).  Returns GQA_OK or
+ * GQA_ERR_INVALID.  Meant for tests and tuning.
  */
 int gqa_prefill_force_block_n(int block_n);
 

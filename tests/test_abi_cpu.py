@@ -102,7 +102,7 @@ def test_plan_is_host_only(lib):
 
 
 def test_force_block_n_validates(lib):
-    assert lib.gqa_prefill_force_block_n(96) == -1
+    assert lib.gqa_prefill_force_block_n(80) == -1
     assert lib.gqa_prefill_force_block_n(64) == 0
     assert lib.gqa_prefill_force_block_n(0) == 0
 

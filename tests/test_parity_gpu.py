@@ -63,7 +63,7 @@ def test_group_sizes(pkg, hq, hkv):
     _check_full(pkg, b)
 
 
-@pytest.mark.parametrize("d,block_n", [(64, 64), (64, 128), (128, 64), (128, 128), (256, 64)])
+@pytest.mark.parametrize("d,block_n", [(64, 64), (64, 96), (64, 128), (128, 64), (128, 128), (256, 64)])
 @pytest.mark.parametrize("window", [0, 100])
 def test_block_n_variants(pkg, d, block_n, window):
     pkg.force_block_n(block_n)
