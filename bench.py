@@ -87,13 +87,14 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (arrival time, line)
+        self.window = None  # (start, end) of the timed region, perf_counter seconds
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -104,7 +105,11 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark(self, start, end):
+        """Keep only samples that arrived inside the timed region."""
+        self.window = (start, end)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -118,7 +123,9 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for when, line in self.lines:
+            if self.window is not None and not (self.window[0] <= when <= self.window[1] + 0.06):
+                continue
             parts = [x.strip() for x in line.split(",")]
             if len(parts) != 6:
                 continue
@@ -211,6 +218,7 @@ def run_ours(args, rank, world):
             ev[i][2].record(stream)
         torch.cuda.synchronize()
         t_wall1 = time.perf_counter()
+        clk.mark(t_wall0, t_wall1)
     dist_barrier(world)
     t_full = [e[0].elapsed_time(e[1]) for e in ev]
     t_win = [e[1].elapsed_time(e[2]) for e in ev]
@@ -236,13 +244,35 @@ def run_ours(args, rank, world):
     h2d = sum(t.numel() * t.element_size() for hb in host for t in hb.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out + host_lse)
 
+    # Three streams, as a caller would pipeline it: host->device copies of the
+    # next layer's inputs and device->host copies of the previous layer's
+    # outputs overlap the current layer's kernel.  Events keep every buffer
+    # reuse ordered across layers and steps.
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+    n_l = len(layers)
+    in_ready = [torch.cuda.Event() for _ in range(n_l)]
+    in_free = [torch.cuda.Event() for _ in range(n_l)]   # kernel done reading inputs
+    out_free = [torch.cuda.Event() for _ in range(n_l)]  # copy-out done reading outputs
+    for e in in_free + out_free:
+        e.record(stream)
+
     def e2e_step():
-        for hb, b, o, l, ho, hl in zip(host, layers, outs, lses, host_out, host_lse):
-            for n, t in hb.items():
-                getattr(b, n).copy_(t, non_blocking=True)
+        for L, (hb, b) in enumerate(zip(host, layers)):
+            h2d_s.wait_event(in_free[L])
+            with torch.cuda.stream(h2d_s):
+                for n, t in hb.items():
+                    getattr(b, n).copy_(t, non_blocking=True)
+            in_ready[L].record(h2d_s)
+        for L, (b, o, l, ho, hl) in enumerate(zip(layers, outs, lses, host_out, host_lse)):
+            stream.wait_event(in_ready[L])
+            stream.wait_event(out_free[L])
             pkg.prefill(b, out=o, lse=l, stream=stream)
-            ho.copy_(o, non_blocking=True)
-            hl.copy_(l, non_blocking=True)
+            in_free[L].record(stream)
+            d2h_s.wait_event(in_free[L])
+            with torch.cuda.stream(d2h_s):
+                ho.copy_(o, non_blocking=True)
+                hl.copy_(l, non_blocking=True)
+            out_free[L].record(d2h_s)
 
     e2e_steps = max(3, min(args.steps, 50))
     for _ in range(3):
@@ -252,8 +282,12 @@ def run_ours(args, rank, world):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    h2d_s.wait_event(e0)
+    d2h_s.wait_event(e0)
     for _ in range(e2e_steps):
         e2e_step()
+    for e in out_free:
+        stream.wait_event(e)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = dist_max(e0.elapsed_time(e1) / e2e_steps, world)
@@ -278,7 +312,8 @@ def run_ours(args, rank, world):
                      "traffic": recorded_traffic(), "peak_source": peaks["source"] + " burst bf16"},
         "e2e": {"value": round(world * sum(flops) / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "pipeline": "copies in / kernel / copies out on three streams, overlapped across layers"},
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
         "timed_wall_s": round(t_wall1 - t_wall0, 3),
@@ -342,12 +377,14 @@ def run_workload(args, rank, world):
     dist_barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
         for i in range(args.steps):
             flush.fill_(float(i))
             ev[i][0].record(stream)
             step()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
+        clk.mark(t0, time.perf_counter())
     dist_barrier(world)
     ms_step = dist_max(statistics.mean(e[0].elapsed_time(e[1]) for e in ev), world)
     peaks = load_peaks()
@@ -376,19 +413,33 @@ def run_workload(args, rank, world):
     return line
 
 
-def oracle_sample_run(layers_cpu, rows_per_layer, offset=0):
+def oracle_inputs(layers_cpu):
+    """Widen each layer's inputs to float64 once, outside any timing."""
+    import numpy as np
+    out = []
+    for b in layers_cpu:
+        x = {n: np.ascontiguousarray(getattr(b, n).double().numpy()) for n in ("q", "k", "v")}
+        x["out"] = np.empty(x["q"].shape)            # result buffers, reused by every call
+        x["lse"] = np.empty(x["q"].shape[:2])
+        out.append((b, x))
+    return out
+
+
+def oracle_sample_run(layers64, rows_per_layer, offset=0):
     """Runs the CPU oracle on `rows_per_layer` evenly spaced query rows of
-    each layer; returns (seconds, useful flops, rows)."""
+    each layer (inputs from oracle_inputs); returns (seconds, useful flops,
+    rows)."""
     import numpy as np
     import oracle
     total_s, total_flops, total_rows = 0.0, 0.0, 0
-    for b in layers_cpu:
+    for b, x in layers64:
         e = b.total_q
         step = max(1, e // rows_per_layer)
         rows = (np.arange(rows_per_layer) * step + offset) % e
         t0 = time.perf_counter()
-        oracle.prefill(b.q, b.k, b.v, b.cu_seqlens_q, b.prefix_lens, b.kv_indptr,
-                       b.scale, b.window, sinks=b.sinks, smooth_softmax=b.smooth, rows=rows)
+        oracle.prefill(x["q"], x["k"], x["v"], b.cu_seqlens_q, b.prefix_lens, b.kv_indptr,
+                       b.scale, b.window, sinks=b.sinks, smooth_softmax=b.smooth, rows=rows,
+                       out=x["out"], lse=x["lse"])
         total_s += time.perf_counter() - t0
         pre = int(b.prefix_lens[0])
         for r in rows:
@@ -398,12 +449,12 @@ def oracle_sample_run(layers_cpu, rows_per_layer, offset=0):
     return total_s, total_flops, total_rows
 
 
-def size_oracle_sample(layers_cpu, target_s):
+def size_oracle_sample(layers64, target_s):
     """Rows per layer so that one oracle sample takes about target_s."""
     probe = 32
-    t, _, _ = oracle_sample_run(layers_cpu, probe)
+    t, _, _ = oracle_sample_run(layers64, probe)
     per_row = max(t / probe, 1e-6)
-    return int(max(8, min(layers_cpu[0].total_q, target_s / per_row)))
+    return int(max(8, min(layers64[0][0].total_q, target_s / per_row)))
 
 
 def cpu_baseline(args):
@@ -411,8 +462,9 @@ def cpu_baseline(args):
     from gqa_flash_attention_prefill_gb300 import workloads as W
     oracle.build()
     layers_cpu = W.layer_pair(seq=args.seq, seed=1)
-    rows = size_oracle_sample(layers_cpu, args.cpu_seconds)
-    t, fl, n = oracle_sample_run(layers_cpu, rows)
+    layers64 = oracle_inputs(layers_cpu)
+    rows = size_oracle_sample(layers64, args.cpu_seconds)
+    t, fl, n = oracle_sample_run(layers64, rows)
     return {"value": fl / t / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
             "kind": "oracle",
             "sample": f"{rows} evenly spaced query rows of each layer (of {layers_cpu[0].total_q}), "
@@ -428,13 +480,15 @@ def run_reference(args, rank, world):
     from gqa_flash_attention_prefill_gb300 import workloads as W
     oracle.build()
     layers_cpu = W.layer_pair(seq=args.seq, seed=1)
-    per_step_s = max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
-    rows = size_oracle_sample(layers_cpu, per_step_s)
+    layers64 = oracle_inputs(layers_cpu)
+    # About 150 s of oracle work in total, however many steps are asked for.
+    per_step_s = max(0.005, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    rows = size_oracle_sample(layers64, per_step_s)
     for i in range(args.warmup):
-        oracle_sample_run(layers_cpu, rows, offset=i)
+        oracle_sample_run(layers64, rows, offset=i)
     secs, fl_total = 0.0, 0.0
     for i in range(args.steps):
-        t, fl, n = oracle_sample_run(layers_cpu, rows, offset=args.warmup + i)
+        t, fl, n = oracle_sample_run(layers64, rows, offset=args.warmup + i)
         secs += t
         fl_total += fl
     value = fl_total / secs / 1e12
@@ -457,7 +511,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--seq", type=int, default=4096)

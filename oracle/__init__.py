@@ -126,10 +126,12 @@ def num_threads() -> int:
 
 
 def prefill(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, scale, window=0,
-            sinks=None, smooth_softmax=False, rows=None, lib=None):
+            sinks=None, smooth_softmax=False, rows=None, lib=None, out=None, lse=None):
     """Run the oracle.  q [total_q,Hq,d]; k,v [total_kv,Hkv,d]; metadata as
     int arrays.  ``rows`` optionally lists the token rows to compute (the
-    others come back as NaN).  Returns (out float64 [total_q,Hq,d],
+    others come back as NaN, or untouched when ``out``/``lse`` are given:
+    caller-owned contiguous float64 buffers of the result shapes, reused
+    across calls).  Returns (out float64 [total_q,Hq,d],
     lse float64 [total_q,Hq])."""
     lib = lib or load()
     q64, k64, v64 = _as_f64(q), _as_f64(k), _as_f64(v)
@@ -138,8 +140,12 @@ def prefill(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, scale, window=0,
     total_kv, hkv, dk = k64.shape
     assert dk == d and v64.shape == k64.shape
     num_seqs = len(pre)
-    out = np.full((total_q, hq, d), np.nan)
-    lse = np.full((total_q, hq), np.nan)
+    if out is None:
+        out = np.full((total_q, hq, d), np.nan)
+    if lse is None:
+        lse = np.full((total_q, hq), np.nan)
+    assert out.dtype == np.float64 and out.shape == (total_q, hq, d) and out.flags.c_contiguous
+    assert lse.dtype == np.float64 and lse.shape == (total_q, hq) and lse.flags.c_contiguous
     sel = None
     if rows is not None:
         sel = np.zeros(total_q, dtype=np.uint8)
