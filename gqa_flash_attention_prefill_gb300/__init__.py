@@ -13,7 +13,7 @@ import os
 from typing import Optional
 
 __all__ = ["load", "gqa_flash_prefill", "gqa_flash_prefill_debug", "prefill",
-           "plan", "force_block_n", "get_device_status", "set_tuning",
+           "plan", "force_block_n", "force_q_tiles", "get_device_status", "set_tuning",
            "clear_config_cache", "config_block_n", "selftest_timeout", "GQAError",
            "GQA_F16", "GQA_BF16", "GQA_DEV_TIMEOUT", "GQA_DEV_BAD_METADATA",
            "EXPORTED_SYMBOLS"]
@@ -27,7 +27,7 @@ EXPORTED_SYMBOLS = [
     "gqa_prefill_force_block_n", "gqa_prefill_get_device_status",
     "gqa_prefill_status_string", "gqa_prefill_version", "gqa_prefill_set_tuning",
     "gqa_prefill_clear_config_cache", "gqa_prefill_config_block_n",
-    "gqa_prefill_selftest_timeout",
+    "gqa_prefill_selftest_timeout", "gqa_prefill_force_q_tiles",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -44,7 +44,8 @@ class GQAError(RuntimeError):
 class _Plan(ctypes.Structure):
     _fields_ = [("rows_per_unit", ctypes.c_int), ("block_n", ctypes.c_int),
                 ("kv_stages", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
-                ("grid", ctypes.c_int), ("max_units", ctypes.c_int)]
+                ("grid", ctypes.c_int), ("max_units", ctypes.c_int),
+                ("q_tiles", ctypes.c_int)]
 
 
 def load(path: Optional[str] = None):
@@ -71,6 +72,8 @@ def load(path: Optional[str] = None):
     lib.gqa_prefill_plan.restype = ctypes.c_int
     lib.gqa_prefill_force_block_n.argtypes = [ctypes.c_int]
     lib.gqa_prefill_force_block_n.restype = ctypes.c_int
+    lib.gqa_prefill_force_q_tiles.argtypes = [ctypes.c_int]
+    lib.gqa_prefill_force_q_tiles.restype = ctypes.c_int
     lib.gqa_prefill_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
     lib.gqa_prefill_get_device_status.restype = ctypes.c_int
     lib.gqa_prefill_status_string.argtypes = [ctypes.c_int]
@@ -82,7 +85,7 @@ def load(path: Optional[str] = None):
     lib.gqa_prefill_clear_config_cache.argtypes = []
     lib.gqa_prefill_clear_config_cache.restype = ctypes.c_int
     lib.gqa_prefill_config_block_n.argtypes = [ctypes.c_int] * 7 + [
-        ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
+        ctypes.POINTER(ctypes.c_int)] * 3
     lib.gqa_prefill_config_block_n.restype = ctypes.c_int
     lib.gqa_prefill_selftest_timeout.argtypes = [ctypes.c_int, ctypes.c_void_p,
                                                  ctypes.POINTER(ctypes.c_int)]
@@ -184,7 +187,7 @@ def prefill(batch, out=None, lse=None, with_lse=True, stream=None):
 
 def plan(num_seqs, total_q, max_seqlen_q, hq, hkv, d, dtype, window) -> dict:
     """Host-only launch plan (rows_per_unit, block_n, kv_stages, ctas_per_sm,
-    grid, max_units) for a call with these shapes."""
+    grid, max_units, q_tiles) for a call with these shapes."""
     p = _Plan()
     code = dtype if isinstance(dtype, int) else (GQA_BF16 if "bf16" in str(dtype) else GQA_F16)
     rc = load().gqa_prefill_plan(int(num_seqs), int(total_q), int(max_seqlen_q), int(hq),
@@ -200,6 +203,13 @@ def force_block_n(block_n: int) -> None:
         raise GQAError(rc, "gqa_prefill_force_block_n")
 
 
+def force_q_tiles(q_tiles: int) -> None:
+    """Pin 1 or 2 query tiles per work unit for later calls (0: the cache's choice)."""
+    rc = load().gqa_prefill_force_q_tiles(int(q_tiles))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_prefill_force_q_tiles")
+
+
 def set_tuning(enable: bool) -> None:
     """Turn the configuration cache's timed sweep on or off (see gqa_prefill.h)."""
     rc = load().gqa_prefill_set_tuning(1 if enable else 0)
@@ -212,15 +222,16 @@ def clear_config_cache() -> None:
 
 
 def config_block_n(total_q, max_seqlen_q, hq, hkv, d, dtype, window):
-    """(block_n, tuned) cached for these shapes; block_n 0 = no entry yet."""
-    bn, tuned = ctypes.c_int(0), ctypes.c_int(0)
+    """(block_n, q_tiles, tuned) cached for these shapes; block_n 0 = no entry
+    yet."""
+    bn, qt, tuned = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
     code = dtype if isinstance(dtype, int) else (GQA_BF16 if "bf16" in str(dtype) else GQA_F16)
     rc = load().gqa_prefill_config_block_n(int(total_q), int(max_seqlen_q), int(hq), int(hkv),
                                            int(d), code, int(window), ctypes.byref(bn),
-                                           ctypes.byref(tuned))
+                                           ctypes.byref(qt), ctypes.byref(tuned))
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_prefill_config_block_n")
-    return bn.value, bool(tuned.value)
+    return bn.value, qt.value, bool(tuned.value)
 
 
 def selftest_timeout(timeout_ms: int = 50, stream=None) -> int:

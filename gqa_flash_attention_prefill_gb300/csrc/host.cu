@@ -37,9 +37,10 @@ __global__ void selftest_wait_kernel(unsigned int* status, unsigned long long ti
 
 namespace {
 
-std::mutex g_mu;      // guards the configuration cache and the forced tile size
+std::mutex g_mu;      // guards the configuration cache and the forced variant
 std::mutex g_dev_mu;  // guards the per-device information
 int g_forced_block_n = 0;
+int g_forced_q_tiles = 0;  // query tiles per unit (0: the cache's choice)
 
 struct DeviceInfo {
   int sms = 0;
@@ -57,7 +58,8 @@ std::map<int, DeviceInfo> g_devices;
 using CfgKey = std::tuple<int, int, int, int, int, int>;
 struct CfgEntry {
   int block_n;
-  bool tuned;  // chosen by a timed sweep rather than the default
+  int q_tiles;  // 128-row query tiles per unit
+  bool tuned;   // chosen by a timed sweep rather than the default
 };
 std::map<CfgKey, CfgEntry> g_cfg_cache;
 int g_tune_mode = -1;  // -1: read GQA_PREFILL_TUNE on first use; 0 off; 1 on
@@ -117,14 +119,16 @@ int pow2_bucket(int x) {
 // Measured on GB300 (gpt-oss layer pair and chunked-prefix workloads): a
 // full-causal d=64 layer runs fastest with 128-key tiles; windowed layers with
 // 64-key tiles, which waste fewer masked keys at the window's lower edge.
-int default_block_n(int d, bool windowed) {
-  if (d == 64) return windowed ? 64 : 128;
-  return 64;
+CfgEntry default_config(int d, bool windowed) {
+  if (d == 64) return CfgEntry{windowed ? 64 : 128, 1, false};
+  return CfgEntry{64, 1, false};
 }
 
 struct Plan {
   KernelShape shape;
-  int rows, G, ctas_per_sm, grid, max_units;
+  int rows;       // query positions per 128-row query tile (128 / G)
+  int unit_rows;  // query positions per unit (q_tiles * rows)
+  int G, ctas_per_sm, grid, max_units;
   unsigned smem_launch;  // dynamic smem requested per CTA
 };
 
@@ -133,17 +137,18 @@ CfgKey cfg_key(int d, int total_q, int max_seqlen_q, int Hq, int G, int window, 
                 window > 0 ? 1 : 0, dtype};
 }
 
-// Plan for an explicit tile size (block_n > 0) or the cache's choice (0).
+// Plan for an explicit variant (block_n > 0, q_tiles > 0) or the cache's
+// choice (0, 0).
 int make_plan_bn(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, int d, int dtype,
-                 int window, int force_bn, Plan* pl);
+                 int window, int force_bn, int force_qt, Plan* pl);
 
 int make_plan(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, int d, int dtype,
               int window, Plan* pl) {
-  return make_plan_bn(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, 0, pl);
+  return make_plan_bn(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, 0, 0, pl);
 }
 
 int make_plan_bn(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, int d, int dtype,
-                 int window, int force_bn, Plan* pl) {
+                 int window, int force_bn, int force_qt, Plan* pl) {
   if (num_seqs < 0 || total_q < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0)
     return GQA_ERR_INVALID;
   if (dtype != GQA_F16 && dtype != GQA_BF16) return GQA_ERR_INVALID;
@@ -153,24 +158,29 @@ int make_plan_bn(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, i
   if (num_seqs > kMaxSeqs) return GQA_ERR_UNSUPPORTED;
   DeviceInfo di;
   const bool have_dev = device_info(&di) == GQA_OK;
-  int bn = force_bn;
-  if (bn == 0) {
+  int bn = force_bn, qt = force_qt;
+  bool qt_pinned = force_qt != 0;
+  if (bn == 0 || qt == 0) {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (g_forced_block_n != 0) {
-      bn = g_forced_block_n;
-    } else {
-      const CfgKey key = cfg_key(d, total_q, max_seqlen_q, Hq, G, window, dtype);
-      auto itr = g_cfg_cache.find(key);
-      if (itr == g_cfg_cache.end())
-        itr = g_cfg_cache.emplace(key, CfgEntry{default_block_n(d, window > 0), false}).first;
-      bn = itr->second.block_n;
+    const CfgKey key = cfg_key(d, total_q, max_seqlen_q, Hq, G, window, dtype);
+    auto itr = g_cfg_cache.find(key);
+    if (itr == g_cfg_cache.end()) itr = g_cfg_cache.emplace(key, default_config(d, window > 0)).first;
+    if (bn == 0) bn = g_forced_block_n != 0 ? g_forced_block_n : itr->second.block_n;
+    if (qt == 0) {
+      qt_pinned = g_forced_q_tiles != 0;
+      qt = qt_pinned ? g_forced_q_tiles : itr->second.q_tiles;
     }
   }
-  if (!kernel_shape(d, bn, &pl->shape)) return GQA_ERR_UNSUPPORTED;
+  // A cached query-tile count that the tile size has no kernel for falls back
+  // to one tile per unit; a pinned one is declined.
+  if (!kernel_shape(d, bn, qt, &pl->shape) &&
+      (qt_pinned || !kernel_shape(d, bn, 1, &pl->shape)))
+    return GQA_ERR_UNSUPPORTED;
   pl->G = G;
   pl->rows = 128 / G;
+  pl->unit_rows = pl->shape.q_tiles * pl->rows;
   const long long max_units =
-      (long long)Hkv * ((total_q + pl->rows - 1) / pl->rows + (long long)num_seqs);
+      (long long)Hkv * ((total_q + pl->unit_rows - 1) / pl->unit_rows + (long long)num_seqs);
   if (max_units > (1ll << 30)) return GQA_ERR_UNSUPPORTED;
   pl->max_units = (int)max_units;
   const int by_tmem = 512 / pl->shape.tmem_cols;
@@ -257,18 +267,18 @@ int launch_planned(const Plan& pl, const void* q, const void* k, const void* v,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (d == 64)
-    e = launch_d64(p, pl.shape.block_n, win, bf16, pl.grid, pl.smem_launch, st);
+    e = launch_d64(p, pl.shape, win, bf16, pl.grid, pl.smem_launch, st);
   else if (d == 128)
-    e = launch_d128(p, pl.shape.block_n, win, bf16, pl.grid, pl.smem_launch, st);
+    e = launch_d128(p, pl.shape, win, bf16, pl.grid, pl.smem_launch, st);
   else
-    e = launch_d256(p, pl.shape.block_n, win, bf16, pl.grid, pl.smem_launch, st);
+    e = launch_d256(p, pl.shape, win, bf16, pl.grid, pl.smem_launch, st);
   if (env_flag("GQA_PREFILL_DEBUG"))
     std::fprintf(stderr,
                  "[gqa_prefill] B=%d total_q=%d total_kv=%d Hq=%d Hkv=%d d=%d %s window=%d "
-                 "sink=%s block_n=%d stages=%d grid=%d (%d/SM) max_units=%d -> %s\n",
+                 "sink=%s block_n=%d q_tiles=%d stages=%d grid=%d (%d/SM) max_units=%d -> %s\n",
                  num_seqs, total_q, total_kv, Hq, Hkv, d, bf16 ? "bf16" : "f16", p.window,
                  sinks ? "head" : (p.smooth ? "smooth" : "none"), pl.shape.block_n,
-                 pl.shape.kv_stages, pl.grid, pl.ctas_per_sm, pl.max_units,
+                 pl.shape.q_tiles, pl.shape.kv_stages, pl.grid, pl.ctas_per_sm, pl.max_units,
                  e == cudaSuccess ? "launched" : cudaGetErrorString(e));
   return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
@@ -281,8 +291,9 @@ int tune_mode() {
 
 // The configuration cache's sweep ([HIPEP] config-cache commit: one sweep per
 // key and process; tuning launches omit the sink, which cannot reorder the
-// candidates): times every candidate tile size on the caller's stream and
-// keeps the fastest.  Synchronises the stream; skipped while capturing.
+// candidates): times every candidate variant (key-tile size x query tiles per
+// unit) on the caller's stream and keeps the fastest.  Synchronises the
+// stream; skipped while capturing.
 int tune_key(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
              const int32_t* prefix_lens, const int32_t* kv_indptr, int num_seqs, int total_q,
              int total_kv, int max_seqlen_q, int Hq, int Hkv, int d, int dtype, float scale,
@@ -291,8 +302,8 @@ int tune_key(const void* q, const void* k, const void* v, const int32_t* cu_seql
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(st, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
     return GQA_OK;
-  const int cands[3] = {64, 96, 128};
-  int best = 0;
+  const int cands[5][2] = {{64, 1}, {96, 1}, {128, 1}, {64, 2}, {128, 2}};
+  int best = 0, best_qt = 0;
   float best_ms = 0.f;
   cudaEvent_t e0, e1;
   if (cudaEventCreate(&e0) != cudaSuccess) return GQA_ERR_CUDA;
@@ -301,11 +312,12 @@ int tune_key(const void* q, const void* k, const void* v, const int32_t* cu_seql
     return GQA_ERR_CUDA;
   }
   int rc = GQA_OK;
-  for (int bn : cands) {
+  for (const auto& cand : cands) {
+    const int bn = cand[0], qt = cand[1];
     Plan pl;
     KernelShape ks;
-    if (!kernel_shape(d, bn, &ks)) continue;
-    rc = make_plan_bn(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, bn, &pl);
+    if (!kernel_shape(d, bn, qt, &ks)) continue;
+    rc = make_plan_bn(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, bn, qt, &pl);
     if (rc != GQA_OK) break;
     auto once = [&]() {
       return launch_planned(pl, q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs, total_q,
@@ -324,11 +336,14 @@ int tune_key(const void* q, const void* k, const void* v, const int32_t* cu_seql
     cudaEventElapsedTime(&ms, e0, e1);
     ms /= 3.f;
     if (env_flag("GQA_PREFILL_TUNE_DEBUG"))
-      std::fprintf(stderr, "[gqa_prefill tune] d=%d sq<=%d Hq=%d G=%d windowed=%d block_n=%d: %.4f ms\n",
+      std::fprintf(stderr,
+                   "[gqa_prefill tune] d=%d sq<=%d Hq=%d G=%d windowed=%d block_n=%d q_tiles=%d: "
+                   "%.4f ms\n",
                    d, pow2_bucket(max_seqlen_q > 0 ? max_seqlen_q : total_q), Hq, Hq / Hkv,
-                   window > 0 ? 1 : 0, bn, ms);
+                   window > 0 ? 1 : 0, bn, qt, ms);
     if (best == 0 || ms < best_ms) {
       best = bn;
+      best_qt = qt;
       best_ms = ms;
     }
   }
@@ -338,7 +353,7 @@ int tune_key(const void* q, const void* k, const void* v, const int32_t* cu_seql
   if (best != 0) {
     std::lock_guard<std::mutex> lk(g_mu);
     g_cfg_cache[cfg_key(d, total_q, max_seqlen_q, Hq, Hq / Hkv, window, dtype)] =
-        CfgEntry{best, true};
+        CfgEntry{best, best_qt, true};
   }
   return GQA_OK;
 }
@@ -364,7 +379,7 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q
     bool need = false;
     {
       std::lock_guard<std::mutex> lk(g_mu);
-      if (g_forced_block_n == 0) {
+      if (g_forced_block_n == 0 && g_forced_q_tiles == 0) {
         auto itr = g_cfg_cache.find(cfg_key(d, total_q, max_seqlen_q, Hq, Hq / Hkv, window, dtype));
         need = itr == g_cfg_cache.end() || !itr->second.tuned;
       }
@@ -386,18 +401,29 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q
 
 }  // namespace
 
-bool kernel_shape(int d, int block_n, KernelShape* out) {
+bool kernel_shape(int d, int block_n, int q_tiles, KernelShape* out) {
   KernelShape s;
   s.block_n = block_n;
-  if (d == 64 && block_n == 128) { s.kv_stages = 2; s.min_blocks = 2; }
-  else if (d == 64 && block_n == 64) { s.kv_stages = 4; s.min_blocks = 2; }
-  else if (d == 64 && block_n == 96) { s.kv_stages = 2; s.min_blocks = 2; }
-  else if (d == 128 && block_n == 64) { s.kv_stages = 2; s.min_blocks = 2; }
-  else if (d == 128 && block_n == 128) { s.kv_stages = 2; s.min_blocks = 1; }
-  else if (d == 256 && block_n == 64) { s.kv_stages = 2; s.min_blocks = 1; }
-  else return false;
-  s.smem = smem_bytes_for(d, block_n, s.kv_stages);
-  s.tmem_cols = tmem_cols_for(d, block_n);
+  s.q_tiles = q_tiles;
+  const int bn = block_n;
+  if (q_tiles == 1) {
+    if (d == 64 && bn == 128) { s.kv_stages = 2; s.min_blocks = 2; }
+    else if (d == 64 && bn == 64) { s.kv_stages = 4; s.min_blocks = 2; }
+    else if (d == 64 && bn == 96) { s.kv_stages = 2; s.min_blocks = 2; }
+    else if (d == 128 && bn == 64) { s.kv_stages = 2; s.min_blocks = 2; }
+    else if (d == 128 && bn == 128) { s.kv_stages = 2; s.min_blocks = 1; }
+    else if (d == 256 && bn == 64) { s.kv_stages = 2; s.min_blocks = 1; }
+    else return false;
+  } else if (q_tiles == 2) {
+    if (d == 64 && bn == 128) { s.kv_stages = 4; s.min_blocks = 1; }
+    else if (d == 64 && bn == 64) { s.kv_stages = 8; s.min_blocks = 1; }
+    else if (d == 128 && bn == 64) { s.kv_stages = 4; s.min_blocks = 1; }
+    else return false;
+  } else {
+    return false;
+  }
+  s.smem = smem_bytes_for(d, block_n, s.kv_stages, q_tiles);
+  s.tmem_cols = tmem_alloc_for(d, block_n, q_tiles);
   *out = s;
   return true;
 }
@@ -435,8 +461,9 @@ int gqa_prefill_plan(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hk
   const int rc =
       gqa::make_plan(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, &pl);
   if (rc != GQA_OK) return rc;
-  plan->rows_per_unit = pl.rows;
+  plan->rows_per_unit = pl.unit_rows;
   plan->block_n = pl.shape.block_n;
+  plan->q_tiles = pl.shape.q_tiles;
   plan->kv_stages = pl.shape.kv_stages;
   plan->ctas_per_sm = pl.ctas_per_sm;
   plan->grid = pl.grid;
@@ -458,7 +485,7 @@ int gqa_prefill_clear_config_cache(void) {
 }
 
 int gqa_prefill_config_block_n(int total_q, int max_seqlen_q, int Hq, int Hkv, int d, int dtype,
-                               int window, int* block_n, int* tuned) {
+                               int window, int* block_n, int* q_tiles, int* tuned) {
   if (block_n == nullptr || tuned == nullptr || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
     return GQA_ERR_INVALID;
   std::lock_guard<std::mutex> lk(gqa::g_mu);
@@ -467,9 +494,11 @@ int gqa_prefill_config_block_n(int total_q, int max_seqlen_q, int Hq, int Hkv, i
   if (itr == gqa::g_cfg_cache.end()) {
     *block_n = 0;
     *tuned = 0;
+    if (q_tiles != nullptr) *q_tiles = 0;
   } else {
     *block_n = itr->second.block_n;
     *tuned = itr->second.tuned ? 1 : 0;
+    if (q_tiles != nullptr) *q_tiles = itr->second.q_tiles;
   }
   return GQA_OK;
 }
@@ -490,6 +519,13 @@ int gqa_prefill_force_block_n(int block_n) {
   if (block_n != 0 && block_n != 64 && block_n != 96 && block_n != 128) return GQA_ERR_INVALID;
   std::lock_guard<std::mutex> lk(gqa::g_mu);
   gqa::g_forced_block_n = block_n;
+  return GQA_OK;
+}
+
+int gqa_prefill_force_q_tiles(int q_tiles) {
+  if (q_tiles < 0 || q_tiles > 2) return GQA_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(gqa::g_mu);
+  gqa::g_forced_q_tiles = q_tiles;
   return GQA_OK;
 }
 

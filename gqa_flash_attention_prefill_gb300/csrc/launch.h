@@ -9,44 +9,47 @@ namespace gqa {
 
 struct KernelShape {
   int block_n;      // keys per tile
+  int q_tiles;      // 128-row query tiles per unit (1, or 2 sharing every K/V tile)
   int kv_stages;    // K/V ring depth
   int min_blocks;   // CTAs per SM the instantiation is compiled for
   unsigned smem;    // dynamic shared memory bytes
   int tmem_cols;    // tensor-memory columns a CTA allocates
 };
 
-// Shape of the instantiation used for (d, block_n); false if none exists.
-bool kernel_shape(int d, int block_n, KernelShape* out);
+// Shape of the instantiation used for (d, block_n, q_tiles); false if none exists.
+bool kernel_shape(int d, int block_n, int q_tiles, KernelShape* out);
 
-// Launches the instantiation for (d, block_n, windowed, bf16) with `grid` CTAs.
+// Launches the instantiation for (d, block_n, q_tiles, windowed, bf16) with `grid` CTAs.
 // `smem` is the dynamic shared memory requested per CTA: at least the
 // instantiation's need, padded so that no more CTAs than planned fit on an SM
 // (each resident CTA holds tensor memory for its whole life).
-cudaError_t launch_d64(const PrefillParams& p, int block_n, bool win, bool bf16, int grid,
-                       unsigned smem, cudaStream_t st);
-cudaError_t launch_d128(const PrefillParams& p, int block_n, bool win, bool bf16, int grid,
-                        unsigned smem, cudaStream_t st);
-cudaError_t launch_d256(const PrefillParams& p, int block_n, bool win, bool bf16, int grid,
-                        unsigned smem, cudaStream_t st);
+cudaError_t launch_d64(const PrefillParams& p, const KernelShape& ks, bool win, bool bf16,
+                       int grid, unsigned smem, cudaStream_t st);
+cudaError_t launch_d64_pair(const PrefillParams& p, const KernelShape& ks, bool win, bool bf16,
+                            int grid, unsigned smem, cudaStream_t st);
+cudaError_t launch_d128(const PrefillParams& p, const KernelShape& ks, bool win, bool bf16,
+                        int grid, unsigned smem, cudaStream_t st);
+cudaError_t launch_d256(const PrefillParams& p, const KernelShape& ks, bool win, bool bf16,
+                        int grid, unsigned smem, cudaStream_t st);
 
-template <int D, int BN, int NS, bool WIN, bool BF16, int MINB>
+template <int D, int BN, int NS, bool WIN, bool BF16, int MINB, int QT>
 cudaError_t launch_one(const PrefillParams& p, int grid, unsigned smem, cudaStream_t st) {
-  auto kern = prefill_kernel<D, BN, NS, WIN, BF16, MINB>;
-  if (smem < smem_bytes_for(D, BN, NS)) return cudaErrorInvalidValue;
+  auto kern = prefill_kernel<D, BN, NS, WIN, BF16, MINB, QT>;
+  if (smem < smem_bytes_for(D, BN, NS, QT)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, st>>>(p);
+  kern<<<grid, threads_for(QT), smem, st>>>(p);
   return cudaGetLastError();
 }
 
-template <int D, int BN, int NS, int MINB>
+template <int D, int BN, int NS, int MINB, int QT>
 cudaError_t launch_variants(const PrefillParams& p, bool win, bool bf16, int grid, unsigned smem,
                             cudaStream_t st) {
   if (win)
-    return bf16 ? launch_one<D, BN, NS, true, true, MINB>(p, grid, smem, st)
-                : launch_one<D, BN, NS, true, false, MINB>(p, grid, smem, st);
-  return bf16 ? launch_one<D, BN, NS, false, true, MINB>(p, grid, smem, st)
-              : launch_one<D, BN, NS, false, false, MINB>(p, grid, smem, st);
+    return bf16 ? launch_one<D, BN, NS, true, true, MINB, QT>(p, grid, smem, st)
+                : launch_one<D, BN, NS, true, false, MINB, QT>(p, grid, smem, st);
+  return bf16 ? launch_one<D, BN, NS, false, true, MINB, QT>(p, grid, smem, st)
+              : launch_one<D, BN, NS, false, false, MINB, QT>(p, grid, smem, st);
 }
 
 }  // namespace gqa

@@ -10,11 +10,17 @@
 // prefix and extend).  The AMD kernels on those pages are prior art only; the
 // structure here is GB300-specific.
 //
-// CTA = 6 warps.  Warps 0-3: softmax + epilogue, thread r owns row r of the
-// 128-row tile (tensor-memory lane r).  Warp 4: TMA producer.  Warp 5: tensor
-// memory allocation and the single-thread MMA issuer.
+// A work unit is QT consecutive 128-row query tiles of one KV head (QT = 1
+// or 2).  With QT = 2 both tiles walk the same key tiles, so every K/V tile
+// brought into shared memory serves 256 rows: half the L2 traffic per flop of
+// QT = 1, and one CTA per SM can keep a K/V ring twice as deep.
 //
-// Row packing: row r of a unit's tile is query head g*G + (r % G) at query
+// CTA = 4*QT + 2 warps.  Warps 0 .. 4*QT-1: softmax + epilogue; warpgroup t
+// (warps 4t .. 4t+3) owns query tile t, thread r of it row r (tensor-memory
+// lane r, in that tile's own 256-column region).  Warp 4*QT: TMA producer.
+// Warp 4*QT+1: tensor memory allocation and the single-thread MMA issuer.
+//
+// Row packing: row r of a query tile is query head g*G + (r % G) at query
 // position q0 + r / G, which is the [token][head] order of q in memory, so
 // one 3-D TMA box (d-chunk, G heads, 128/G tokens) fills the tile and every
 // K/V tile is loaded once for all G heads of the group.
@@ -28,7 +34,9 @@
 namespace gqa {
 
 constexpr int kMaxSeqs = 512;        // sequences per call (shared-memory tables)
-constexpr int kThreads = 192;        // 6 warps
+// Threads per CTA with QT query tiles: a softmax warpgroup per tile, one
+// producer warp and one MMA warp.
+__host__ __device__ constexpr int threads_for(int QT) { return 32 * (4 * QT + 2); }
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // Lazy rescale: the running max used as the exponent reference is only moved
@@ -51,7 +59,7 @@ struct PrefillParams {
   int32_t* unit_log;
   unsigned int* status;
   int num_seqs, total_q, total_kv;
-  int Hq, Hkv, G, rows;  // rows = query positions per unit = 128 / G
+  int Hq, Hkv, G, rows;  // rows = query positions per 128-row query tile = 128 / G
   int window;            // <= 0: none
   int smooth;
   float scale_log2;      // scale * log2(e)
@@ -66,35 +74,41 @@ __host__ __device__ constexpr int pow2_cols(int n) {
 __host__ __device__ constexpr int p_buffers(int D, int BN) {
   return pow2_cols(BN + BN + D) == pow2_cols(BN + BN / 2 + D) ? 2 : 1;
 }
-// S (BN fp32 columns) + P buffers (BN 16-bit values = BN/2 columns each) + O (D columns)
+// S (BN fp32 columns) + P buffers (BN 16-bit values = BN/2 columns each) + O
+// (D columns): one query tile's tensor memory.
 __host__ __device__ constexpr int tmem_cols_for(int D, int BN) {
   return pow2_cols(BN + p_buffers(D, BN) * (BN / 2) + D);
+}
+// A CTA's allocation: two query tiles take 256 columns each.
+__host__ __device__ constexpr int tmem_alloc_for(int D, int BN, int QT) {
+  return QT == 1 ? tmem_cols_for(D, BN) : 512;
 }
 
 // Q tiles in flight per CTA: two for d = 64 (the next unit's Q loads during
 // the current unit and two CTAs still fit on an SM), one for larger d.
 __host__ __device__ constexpr int q_buffers(int D) { return D == 64 ? 2 : 1; }
 
-__host__ __device__ constexpr uint32_t smem_bytes_for(int D, int BN, int NS) {
-  return 1024u                                  // alignment slack
-         + (uint32_t)q_buffers(D) * 128u * D * 2u  // Q tiles
-         + 2u * NS * BN * D * 2u                // K and V rings
-         + 64u * 8u                             // mbarriers
-         + 16u                                  // misc words
-         + 4u * (4 * kMaxSeqs + 2)              // per-sequence tables
-         + 4u * 8u;                             // scan scratch (one word per warp)
+__host__ __device__ constexpr uint32_t smem_bytes_for(int D, int BN, int NS, int QT) {
+  return 1024u                                          // alignment slack
+         + (uint32_t)q_buffers(D) * QT * 128u * D * 2u  // Q tiles
+         + 2u * NS * BN * D * 2u                        // K and V rings
+         + 64u * 8u                                     // mbarriers
+         + 16u                                          // misc words
+         + 4u * (4 * kMaxSeqs + 2)                      // per-sequence tables
+         + 4u * 16u;                                    // scan scratch (one word per warp)
 }
 
-// Barrier indices
+// Barrier indices.  Each query tile t has a block of 8 at kSub + 8 t.
 template <int NS>
 struct Bar {
   static constexpr int kQFull = 0, kQEmpty = 2;  // two each (Q double buffer)
   static constexpr int kKFull = 4, kKEmpty = 4 + NS, kVFull = 4 + 2 * NS, kVEmpty = 4 + 3 * NS;
-  static constexpr int kSFull = 4 + 4 * NS, kSFree = kSFull + 1;
-  static constexpr int kPFull = kSFull + 2, kODone = kSFull + 4;  // one per P buffer
-  static constexpr int kDrain = kSFull + 6;
-  static constexpr int kEpi = kSFull + 7;  // output tile staged in shared memory
-  static constexpr int kCount = kSFull + 8;
+  static constexpr int kSub = 4 + 4 * NS;
+  static constexpr int kSFull = 0, kSFree = 1;  // offsets inside a query tile's block
+  static constexpr int kPFull = 2, kODone = 4;  // one per P buffer
+  static constexpr int kEpi = 6;                // output tile staged in shared memory
+  static constexpr int kDrain = kSub + 16;
+  static constexpr int kCount = kDrain + 1;
 };
 
 struct Unit {
@@ -104,17 +118,17 @@ struct Unit {
 // Per-sequence metadata copied into shared memory once per CTA, so that
 // decoding a unit never waits on global memory.
 struct SeqTab {
-  const int32_t* tile_start;  // [B+1] exclusive scan of query tiles per sequence
+  const int32_t* tile_start;  // [B+1] exclusive scan of units per sequence
   const int32_t* cu0;         // [B+1] cu_seqlens_q
   const int32_t* pre;         // [B]   prefix_lens
   const int32_t* kvb;         // [B]   kv_indptr (first key row)
 };
 
-// Unit u -> (sequence, KV head, query tile).  Units are numbered with the KV
-// head fastest and, inside a sequence, the last (costliest under causality)
-// query tile first.
+// Unit u -> (sequence, KV head, unit of `urows` query positions).  Units are
+// numbered with the KV head fastest and, inside a sequence, the last
+// (costliest under causality) unit first.
 __device__ __forceinline__ Unit decode_unit(const PrefillParams& p, const SeqTab& T, int u,
-                                            int BN) {
+                                            int BN, int urows) {
   Unit U;
   U.g = u % p.Hkv;
   const int tau = u / p.Hkv;
@@ -126,11 +140,11 @@ __device__ __forceinline__ Unit decode_unit(const PrefillParams& p, const SeqTab
   U.b = lo;
   const int t = tau - T.tile_start[lo];
   const int tiles_b = T.tile_start[lo + 1] - T.tile_start[lo];
-  U.q0 = (tiles_b - 1 - t) * p.rows;
+  U.q0 = (tiles_b - 1 - t) * urows;
   U.P = T.pre[lo];
   const int cu0 = T.cu0[lo];
   U.E = T.cu0[lo + 1] - cu0;
-  U.q_last = min(U.q0 + p.rows, U.E) - 1;
+  U.q_last = min(U.q0 + urows, U.E) - 1;
   U.q_row0 = cu0 + U.q0;
   U.kv_base = T.kvb[lo];
   const KvRange r = kv_range(U.P, U.q0, U.q_last, p.window, BN);
@@ -186,17 +200,23 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity,
   }
 }
 
-template <int D, int BN, int NS, bool WIN, bool BF16, int MINB>
-__global__ void __launch_bounds__(kThreads, MINB)
+
+template <int D, int BN, int NS, bool WIN, bool BF16, int MINB, int QT>
+__global__ void __launch_bounds__(threads_for(QT), MINB)
     prefill_kernel(const __grid_constant__ PrefillParams p) {
   static_assert(D == 64 || D == 128 || D == 256, "head dim");
   static_assert(BN == 64 || BN == 96 || BN == 128, "key tile");
+  static_assert(QT == 1 || (QT == 2 && tmem_cols_for(D, BN) <= 256), "query tiles per CTA");
+  constexpr int kThr = threads_for(QT);
+  constexpr int kSmWarps = 4 * QT;  // softmax warps
+  constexpr int kProdWarp = kSmWarps, kMmaWarp = kSmWarps + 1;
   constexpr int NCH = D / 64;  // 128-byte swizzle chunks along d
-  constexpr uint32_t kQBytes = 128u * D * 2u;
+  constexpr uint32_t kQBytes = 128u * D * 2u;  // one 128-row query tile
   constexpr uint32_t kKVBytes = (uint32_t)BN * D * 2u;
   constexpr uint32_t kQChunk = 128u * 128u;
   constexpr uint32_t kKVChunk = (uint32_t)BN * 128u;
-  constexpr uint32_t kTmemCols = (uint32_t)tmem_cols_for(D, BN);
+  constexpr uint32_t kTmemCols = (uint32_t)tmem_alloc_for(D, BN, QT);
+  constexpr uint32_t kSubCols = 256u;  // tensor-memory columns between query tiles
   constexpr uint32_t NP = (uint32_t)p_buffers(D, BN);
   constexpr uint32_t kColS = 0, kColP = BN, kColO = BN + NP * (BN / 2);
   constexpr uint32_t kIdescS = idesc_f16(BF16, 128, BN, false);  // Q, K both K-major
@@ -206,11 +226,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  constexpr uint32_t NQ = (uint32_t)q_buffers(D);
-  const uint32_t sQ = smem_u32(smem);  // NQ Q buffers
-  const uint32_t sK = sQ + NQ * kQBytes;
+  constexpr uint32_t NQ = (uint32_t)q_buffers(D);  // Q buffers, each holding QT tiles
+  const uint32_t sQ = smem_u32(smem);
+  const uint32_t sK = sQ + NQ * QT * kQBytes;
   const uint32_t sV = sK + NS * kKVBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NQ * kQBytes + 2 * NS * kKVBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NQ * QT * kQBytes + 2 * NS * kKVBytes);
   const uint32_t sBar = smem_u32(bars);
   uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 64);  // [0] tmem base, [1] abort, [2] bad
   int32_t* tile_start = reinterpret_cast<int32_t*>(misc + 4);
@@ -222,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
   volatile uint32_t* abort_flag = misc + 1;
   const unsigned long long tmo = p.timeout_ns;
   const int win = WIN ? p.window : 0;
+  const int urows = QT * p.rows;  // query positions per unit
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -229,27 +250,30 @@ __global__ void __launch_bounds__(kThreads, MINB)
   if (tid == 0) {
     for (int i = 0; i < B::kCount; ++i) {
       uint32_t cnt = 1u;
-      if (i == B::kSFree || i == B::kPFull || i == B::kPFull + 1 || i == B::kEpi) cnt = 128u;
+      for (int t = 0; t < QT; ++t) {
+        const int o = i - (B::kSub + 8 * t);
+        if (o == B::kSFree || o == B::kPFull || o == B::kPFull + 1 || o == B::kEpi) cnt = 128u;
+      }
       // A Q buffer is free once the unit's last QK^T is done (MMA commit) and
-      // its epilogue has finished staging the output through it (one arrival).
-      if (i == B::kQEmpty || i == B::kQEmpty + 1) cnt = 2u;
+      // each query tile's epilogue has finished staging its output through it.
+      if (i == B::kQEmpty || i == B::kQEmpty + 1) cnt = 1u + QT;
       mbar_init(sBar + 8u * i, cnt);
     }
     misc[1] = 0u;
     misc[2] = 0u;
     fence_barrier_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == kProdWarp && lane == 0) {
     tma_prefetch_desc(&p.tmap_q);
     tma_prefetch_desc(&p.tmap_k);
     tma_prefetch_desc(&p.tmap_v);
   }
   __syncthreads();
 
-  // Per-sequence query-tile counts, their exclusive scan, and the metadata
-  // checks (bad metadata: write nothing, raise GQA_DEV_BAD_METADATA).
+  // Per-sequence unit counts, their exclusive scan, and the metadata checks
+  // (bad metadata: write nothing, raise GQA_DEV_BAD_METADATA).
   const int nseq = p.num_seqs;
-  const int per = (nseq + kThreads - 1) / kThreads;
+  const int per = (nseq + kThr - 1) / kThr;
   const int b_lo = min(tid * per, nseq), b_hi = min(b_lo + per, nseq);
   int local = 0;
   bool bad = (tid == 0) && (__ldg(p.cu_seqlens_q) != 0);
@@ -262,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         (long long)k1 - k0 != (long long)P + E)
       bad = true;
     else
-      local += (E + p.rows - 1) / p.rows;
+      local += (E + urows - 1) / urows;
     seq_cu0[b] = c0;
     seq_pre[b] = P;
     seq_kvb[b] = k0;
@@ -280,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
   __syncthreads();
   if (tid == 0) {
     int acc = 0;
-    for (int w = 0; w < kThreads / 32; ++w) {
+    for (int w = 0; w < kThr / 32; ++w) {
       const int v = scan[w];
       scan[w] = acc;
       acc += v;
@@ -293,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     for (int b = b_lo; b < b_hi; ++b) {
       tile_start[b] = acc;
       const int E = __ldg(p.cu_seqlens_q + b + 1) - __ldg(p.cu_seqlens_q + b);
-      acc += E > 0 ? (E + p.rows - 1) / p.rows : 0;
+      acc += E > 0 ? (E + urows - 1) / urows : 0;
     }
   }
   __syncthreads();
@@ -304,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
   const int n_units = tile_start[nseq] * p.Hkv;
   if (blockIdx.x >= n_units) return;  // nothing for this CTA (before any TMEM use)
 
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(misc), kTmemCols);
     tmem_relinquish();
   }
@@ -316,10 +340,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
   // ---------------------------------------------------------------- producer
   // Two iterators over the CTA's sequence of key tiles: K runs up to one tile
   // ahead of V (a K slot frees when its QK^T is done, a V slot only when its
-  // PV is done), and a unit's Q tile is requested just before its first K.
+  // PV is done), and a unit's Q tiles are requested just before its first K.
   // With a single Q buffer the V iterator first finishes the previous unit,
   // whose epilogue must release that buffer.
-  if (warp == 4) {
+  if (warp == kProdWarp) {
     if (lane == 0) {
       uint32_t nq = 0, nk[NS], nv[NS];
       for (int s = 0; s < NS; ++s) nk[s] = nv[s] = 0u;
@@ -329,17 +353,20 @@ __global__ void __launch_bounds__(kThreads, MINB)
         if (!wait_bounded(sBar + 8u * (B::kQEmpty + qb), ((nq / NQ) & 1u) ^ 1u, abort_flag,
                           p.status, tmo))
           return false;
-        mbar_arrive_expect_tx(sBar + 8u * (B::kQFull + qb), kQBytes);
-        for (int c = 0; c < NCH; ++c)
-          tma_load_3d(sQ + qb * kQBytes + c * kQChunk, &p.tmap_q, sBar + 8u * (B::kQFull + qb),
-                      c * 64, U.g * p.G, U.q_row0);
+        mbar_arrive_expect_tx(sBar + 8u * (B::kQFull + qb), QT * kQBytes);
+        // A query tile past the end of q (a unit's second tile at the end of
+        // the batch) reads the tensor map's zero fill; its rows are never stored.
+        for (int t = 0; t < QT; ++t)
+          for (int c = 0; c < NCH; ++c)
+            tma_load_3d(sQ + (qb * QT + t) * kQBytes + c * kQChunk, &p.tmap_q,
+                        sBar + 8u * (B::kQFull + qb), c * 64, U.g * p.G, U.q_row0 + t * p.rows);
         ++nq;
         return true;
       };
       int kk = 0, jk = 0, uk = unit_of(0);
       uint32_t itk = 0;
       Unit Uk;
-      if (uk < n_units) Uk = decode_unit(p, T, uk, BN);
+      if (uk < n_units) Uk = decode_unit(p, T, uk, BN, urows);
       int kv = 0, jv = 0, uv = uk;
       uint32_t itv = 0;
       Unit Uv = Uk;
@@ -361,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
           if (++jk == Uk.n_tiles) {
             jk = 0;
             uk = unit_of(++kk);
-            if (uk < n_units) Uk = decode_unit(p, T, uk, BN);
+            if (uk < n_units) Uk = decode_unit(p, T, uk, BN, urows);
           }
         } else {
           const uint32_t s = itv % NS, ph = (itv / NS) & 1u;
@@ -377,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
           if (++jv == Uv.n_tiles) {
             jv = 0;
             uv = unit_of(++kv);
-            if (uv < n_units) Uv = decode_unit(p, T, uv, BN);
+            if (uv < n_units) Uv = decode_unit(p, T, uv, BN, urows);
           }
         }
       }
@@ -397,83 +424,95 @@ __global__ void __launch_bounds__(kThreads, MINB)
   }
 
   // ---------------------------------------------------------------- MMA issuer
-  if (warp == 5) {
-    if (lane == 0) {
-      // Q and K: K-major, 128-byte swizzle; the 16-wide k-step advances the
-      // start address by 32 bytes inside a 128-byte swizzle row, the 64-wide
-      // d-chunk by one chunk.  Stride between 8-row groups: 1024 bytes.
-      auto qdesc = [&](uint32_t qb, int kk) {
-        return smem_desc_sw128(sQ + qb * kQBytes + (kk >> 2) * kQChunk + (kk & 3) * 32, 16, 1024);
-      };
-      auto kdesc = [&](uint32_t s, int kk) {
-        return smem_desc_sw128(sK + s * kKVBytes + (kk >> 2) * kKVChunk + (kk & 3) * 32, 16, 1024);
-      };
-      // V: MN-major (d contiguous), 128-byte swizzle; a 16-key step is two
-      // 8-key groups = 2048 bytes; d-chunks of 64 are kKVChunk apart.
-      auto vdesc = [&](uint32_t s, int kk) {
-        return smem_desc_sw128(sV + s * kKVBytes + kk * 2048, kKVChunk, 1024);
-      };
-      auto issue_pv = [&](uint32_t itp, bool first) -> bool {
-        const uint32_t sp = itp % NS, php = (itp / NS) & 1u;
-        if (!wait_bounded(sBar + 8u * (B::kVFull + sp), php, abort_flag, p.status, tmo)) return false;
-        const uint32_t pb = itp % NP;
-        if (!wait_bounded(sBar + 8u * (B::kPFull + pb), (itp / NP) & 1u, abort_flag, p.status, tmo))
-          return false;
+  // The whole warp runs this loop (the MMA helpers issue from one elected
+  // lane), so the waits, the loop and the descriptors stay warp-uniform.
+  if (warp == kMmaWarp) {
+    // Q and K: K-major, 128-byte swizzle; the 16-wide k-step advances the
+    // start address by 32 bytes inside a 128-byte swizzle row, the 64-wide
+    // d-chunk by one chunk.  Stride between 8-row groups: 1024 bytes.
+    // V: MN-major (d contiguous), 128-byte swizzle; a 16-key step is two
+    // 8-key groups = 2048 bytes; d-chunks of 64 are kKVChunk apart.
+    // Shared-memory addresses stay below 2^18, so moving a descriptor to
+    // another buffer or k-step is an add to its start-address field.
+    const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024);
+    const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024);
+    const uint64_t dV0 = smem_desc_sw128(sV, kKVChunk, 1024);
+    auto kstep = [](int kk, uint32_t chunk) -> uint64_t {
+      return (uint64_t)(((uint32_t)(kk >> 2) * chunk + (uint32_t)(kk & 3) * 32u) >> 4);
+    };
+    auto sub_bar = [&](int t, int o) { return sBar + 8u * (B::kSub + 8 * t + o); };
+    auto wait_all = [&](uint32_t bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort_flag, p.status, tmo));
+    };
+    // O_t += P_t V for every query tile t, once V and that tile's P are in.
+    auto issue_pv = [&](uint32_t itp, bool first) -> bool {
+      const uint32_t sp = itp % NS, php = (itp / NS) & 1u;
+      if (!wait_all(sBar + 8u * (B::kVFull + sp), php)) return false;
+      const uint32_t pb = itp % NP;
+      const uint64_t dv = dV0 + sp * (kKVBytes >> 4);
+      for (int t = 0; t < QT; ++t) {
+        if (!wait_all(sub_bar(t, B::kPFull + pb), (itp / NP) & 1u)) return false;
         tc_fence_after();
+        const uint32_t tb = tmem + t * kSubCols;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem + kColO, tmem + kColP + pb * (BN / 2) + kk * 8, vdesc(sp, kk), kIdescO,
-                 (first && kk == 0) ? 0u : 1u);
-        mma_commit(sBar + 8u * (B::kODone + pb));
-        mma_commit(sBar + 8u * (B::kVEmpty + sp));
-        return true;
-      };
-      uint32_t it = 0, uc = 0;
-      bool ok = true;
-      int u = unit_of(0);
-      Unit Un;
-      if (u < n_units) Un = decode_unit(p, T, u, BN);
-      for (int k = 0; ok && u < n_units; ++k) {
-        const Unit U = Un;  // decoded one unit ahead: its loads overlap this unit
-        const int u_next = unit_of(k + 1);
-        if (u_next < n_units) Un = decode_unit(p, T, u_next, BN);
-        u = u_next;
-        const uint32_t qb = uc % NQ;
-        if (!(ok = wait_bounded(sBar + 8u * (B::kQFull + qb), (uc / NQ) & 1u, abort_flag, p.status,
-                                tmo)))
-          break;
-        for (int j = 0; j < U.n_tiles; ++j) {
-          const uint32_t cur = it + j;
-          const uint32_t s = cur % NS, ph = (cur / NS) & 1u;
-          if (!(ok = wait_bounded(sBar + 8u * (B::kKFull + s), ph, abort_flag, p.status, tmo))) break;
-          if (cur > 0 &&
-              !(ok = wait_bounded(sBar + 8u * B::kSFree, (cur - 1u) & 1u, abort_flag, p.status, tmo)))
-            break;
+          mma_ts(tb + kColO, tb + kColP + pb * (BN / 2) + kk * 8, dv + (uint64_t)(kk * 128),
+                 kIdescO, (first && kk == 0) ? 0u : 1u);
+        mma_commit(sub_bar(t, B::kODone + pb));
+      }
+      mma_commit(sBar + 8u * (B::kVEmpty + sp));
+      return true;
+    };
+    uint32_t it = 0, uc = 0;
+    bool ok = true;
+    int u = unit_of(0);
+    Unit Un;
+    if (u < n_units) Un = decode_unit(p, T, u, BN, urows);
+    for (int k = 0; ok && u < n_units; ++k) {
+      const Unit U = Un;  // decoded one unit ahead: its loads overlap this unit
+      const int u_next = unit_of(k + 1);
+      if (u_next < n_units) Un = decode_unit(p, T, u_next, BN, urows);
+      u = u_next;
+      const uint32_t qb = uc % NQ;
+      if (!(ok = wait_all(sBar + 8u * (B::kQFull + qb), (uc / NQ) & 1u))) break;
+      for (int j = 0; j < U.n_tiles; ++j) {
+        const uint32_t cur = it + j;
+        const uint32_t s = cur % NS, ph = (cur / NS) & 1u;
+        const uint64_t dk = dK0 + s * (kKVBytes >> 4);
+        if (!(ok = wait_all(sBar + 8u * (B::kKFull + s), ph))) break;
+        for (int t = 0; t < QT && ok; ++t) {
+          if (cur > 0 && !(ok = wait_all(sub_bar(t, B::kSFree), (cur - 1u) & 1u))) break;
           tc_fence_after();
+          const uint64_t dq = dQ0 + (qb * QT + t) * (kQBytes >> 4);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + kColS, qdesc(qb, kk), kdesc(s, kk), kIdescS, kk > 0 ? 1u : 0u);
-          mma_commit(sBar + 8u * B::kSFull);
-          mma_commit(sBar + 8u * (B::kKEmpty + s));
-          if (j == U.n_tiles - 1) mma_commit(sBar + 8u * (B::kQEmpty + qb));
-          // PV of the previous tile goes after this tile's QK^T, so the
-          // tensor core works on S(j) while the softmax warps work on S(j-1).
-          if (j > 0 && !(ok = issue_pv(cur - 1u, j == 1))) break;
+            mma_ss(tmem + t * kSubCols + kColS, dq + kstep(kk, kQChunk), dk + kstep(kk, kKVChunk),
+                   kIdescS, kk > 0 ? 1u : 0u);
+          mma_commit(sub_bar(t, B::kSFull));
         }
-        if (ok) ok = issue_pv(it + U.n_tiles - 1u, U.n_tiles == 1);
-        it += U.n_tiles;
-        ++uc;
+        if (!ok) break;
+        mma_commit(sBar + 8u * (B::kKEmpty + s));
+        if (j == U.n_tiles - 1) mma_commit(sBar + 8u * (B::kQEmpty + qb));
+        // PV of the previous tile goes after this tile's QK^T, so the
+        // tensor core works on S(j) while the softmax warps work on S(j-1).
+        if (j > 0 && !(ok = issue_pv(cur - 1u, j == 1))) break;
       }
-      mma_commit(sBar + 8u * B::kDrain);  // completes when every MMA issued is done
-      wait_drain(sBar + 8u * B::kDrain, 0u, tmo);
+      if (ok) ok = issue_pv(it + U.n_tiles - 1u, U.n_tiles == 1);
+      it += U.n_tiles;
+      ++uc;
     }
+    mma_commit(sBar + 8u * B::kDrain);  // completes when every MMA issued is done
+    wait_drain(sBar + 8u * B::kDrain, 0u, tmo);
     __syncwarp();
   }
 
   // ---------------------------------------------------------------- softmax + epilogue
-  if (warp < 4) {
-    const int r = tid;  // tile row == tensor-memory lane
-    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+  if (warp < kSmWarps) {
+    const int sub = warp >> 2;        // query tile of this warpgroup
+    const int r = (warp & 3) * 32 + lane;  // tile row == tensor-memory lane
+    const bool leader = r == 0;       // first thread of the warpgroup
+    const uint32_t t_lane = tmem + sub * kSubCols + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t bsub = sBar + 8u * (B::kSub + 8 * sub);  // this tile's barrier block
     const float sl2 = p.scale_log2;
     uint32_t it = 0;
     bool ok = true;
@@ -484,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     Unit Un;
     float sink_next = 0.f;
     if (u < n_units) {
-      Un = decode_unit(p, T, u, BN);
+      Un = decode_unit(p, T, u, BN, urows);
       if (p.sinks != nullptr) sink_next = __ldg(p.sinks + Un.g * p.G + r % p.G);
     }
     for (int k = 0; ok && u < n_units; ++k) {
@@ -496,30 +535,34 @@ __global__ void __launch_bounds__(kThreads, MINB)
       const uint32_t qb = (uint32_t)k % NQ;  // this unit's Q buffer
       u = unit_of(k + 1);
       if (u < n_units) {
-        Un = decode_unit(p, T, u, BN);
+        Un = decode_unit(p, T, u, BN, urows);
         if (p.sinks != nullptr) sink_next = __ldg(p.sinks + Un.g * p.G + r % p.G);
       }
-      const int pl = U.q0 + r / p.G;  // query position inside the sequence
+      // This warpgroup's query tile: positions [q0s, qls] (empty when qls < q0s,
+      // a unit's second tile past the end of its sequence).
+      const int q0s = U.q0 + sub * p.rows;
+      const int qls = min(q0s + p.rows, U.E) - 1;
+      const int pl = q0s + r / p.G;  // query position inside the sequence
       const int h = U.g * p.G + r % p.G;
       const int pos = U.P + pl;
       float m = -INFINITY;  // exponent reference (log2 domain)
       float l = 0.f;        // running denominator, relative to m
-      int n_masked = 0;
+      int n_masked = 0;     // tiles of the unit needing the mask (tile_needs_mask)
       for (int j = 0; j < U.n_tiles; ++j, ++it) {
         const int n0 = U.kv_lo + j * BN;
         ok = __all_sync(0xffffffffu,
-                        wait_bounded(sBar + 8u * B::kSFull, it & 1u, abort_flag, p.status, tmo));
+                        wait_bounded(bsub + 8u * B::kSFull, it & 1u, abort_flag, p.status, tmo));
         if (!ok) break;
         tc_fence_after();
         // The S row is processed in 64-column chunks so that only one chunk
         // of fp32 scores is live in registers; the packed 16-bit P of earlier
         // chunks (half the size) waits in registers until the tile is done.
-        // Edge tests are uniform over the CTA: the causal edge (a key past the
-        // first row's position) and the window edge (a key below the last
-        // row's lower bound); their union is tile_needs_mask().
-        const bool edge_c = n0 + BN - 1 > U.P + U.q0;
-        const bool edge_w = WIN && n0 < U.P + U.q_last - win + 1;
-        n_masked += (edge_c || edge_w) ? 1 : 0;
+        // Edge tests are uniform over the warpgroup: the causal edge (a key
+        // past the tile's first position) and the window edge (a key below
+        // the tile's last position's lower bound).
+        const bool edge_c = n0 + BN - 1 > U.P + q0s;
+        const bool edge_w = WIN && n0 < U.P + qls - win + 1;
+        n_masked += tile_needs_mask(n0, BN, U.P, U.q0, U.q_last, win) ? 1 : 0;
         // S is processed in CW-column chunks (64, or 48 for 96-key tiles).
         constexpr int CW = (BN == 96) ? 48 : 64;
         constexpr int NCK = BN / CW;
@@ -529,15 +572,19 @@ __global__ void __launch_bounds__(kThreads, MINB)
 #pragma unroll
         for (int ch = 0; ch < NCK; ++ch) {
           uint32_t sr[64];
-          tmem_ld32(t_lane + kColS + ch * CW, *reinterpret_cast<uint32_t(*)[32]>(sr));
+          // The reducing load also yields the row maximum of each 32-column
+          // half; it stands for the chunk maximum on tiles without a mask.
+          float red0 = tmem_ld32_max(t_lane + kColS + ch * CW, *reinterpret_cast<uint32_t(*)[32]>(sr));
+          float red1 = -INFINITY;
           if constexpr (CW == 64)
-            tmem_ld32(t_lane + kColS + ch * CW + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+            red1 = tmem_ld32_max(t_lane + kColS + ch * CW + 32,
+                                 *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
           else
             tmem_ld16(t_lane + kColS + ch * CW + 32, *reinterpret_cast<uint32_t(*)[16]>(sr + 32));
           tmem_wait_ld();
           if (ch == NCK - 1) {
             tc_fence_before();
-            mbar_arrive(sBar + 8u * B::kSFree);  // S is in registers: next QK^T may overwrite it
+            mbar_arrive(bsub + 8u * B::kSFree);  // S is in registers: next QK^T may overwrite it
           }
           // Per-element mask on edge tiles only: row `pos` keeps columns
           // [c_lo, c_hi] of this chunk; one-sided tiles test one bound.
@@ -560,16 +607,21 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 if (c < c_lo) sr[c] = __float_as_uint(-INFINITY);
             }
           }
-          // Chunk max over independent chains (short dependency chains).
-          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+          float mx = fmaxf(red0, red1);
+          if (CW != 64 || edge_c || edge_w) {
+            // Masked (or 48-column) chunk: maximum over the kept values, over
+            // independent chains (short dependency chains).
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < CW; c += 8) {
-            mx0 = max3(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
-            mx1 = max3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-            mx2 = max3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
-            mx3 = max3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+            for (int c = 0; c < CW; c += 8) {
+              mx0 = max3(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
+              mx1 = max3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+              mx2 = max3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+              mx3 = max3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+            }
+            mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
           }
-          const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+          const float m_cand = mx * sl2;
           if (m_cand > m + kRescaleThreshold) {  // move the reference (rare after the first tile)
             const float a = ex2(m - m_cand);     // m = -inf gives 0
             alpha *= a;
@@ -612,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         // P buffer `pb` is rewritten once the PV that last read it is done.
         const uint32_t pb = it % NP;
         if (it >= NP)
-          ok = __all_sync(0xffffffffu, wait_bounded(sBar + 8u * (B::kODone + pb),
+          ok = __all_sync(0xffffffffu, wait_bounded(bsub + 8u * (B::kODone + pb),
                                                      ((it / NP) & 1u) ^ 1u, abort_flag, p.status,
                                                      tmo));
         if (!ok) break;
@@ -630,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
           if (NP > 1) {
             const uint32_t prev = it - 1u;
             ok = __all_sync(0xffffffffu,
-                            wait_bounded(sBar + 8u * (B::kODone + prev % NP), (prev / NP) & 1u,
+                            wait_bounded(bsub + 8u * (B::kODone + prev % NP), (prev / NP) & 1u,
                                          abort_flag, p.status, tmo));
             if (!ok) break;
             tc_fence_after();
@@ -648,8 +700,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(sBar + 8u * (B::kPFull + pb));
-        if (release_pending && r == 0) {
+        mbar_arrive(bsub + 8u * (B::kPFull + pb));
+        if (release_pending && leader) {
           // The previous unit's output store has read its staging buffer by now
           // (or shortly); hand that Q buffer back to the producer.
           bulk_wait_group_read0();
@@ -660,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
       if (!ok) break;
 
       // Epilogue: fold the sink into the denominator, normalise, store.
-      ok = __all_sync(0xffffffffu, wait_bounded(sBar + 8u * (B::kODone + (it - 1u) % NP),
+      ok = __all_sync(0xffffffffu, wait_bounded(bsub + 8u * (B::kODone + (it - 1u) % NP),
                                                  ((it - 1u) / NP) & 1u, abort_flag, p.status, tmo));
       if (!ok) break;
       tc_fence_after();
@@ -677,14 +729,15 @@ __global__ void __launch_bounds__(kThreads, MINB)
         inv = a / den;
         lse2 = mf + log2f(den);
       }
-      const bool valid = pl <= U.q_last;
-      const size_t orow = (size_t)(U.q_row0 + r / p.G) * p.Hq + h;
-      // A unit whose rows all belong to its sequence is staged in its own Q
-      // buffer (its last QK^T is done) in the 128-byte-swizzled layout of the
-      // output tensor map and written by one TMA store; a ragged tail unit
-      // stores its valid rows directly.
-      const bool full = (U.q_last - U.q0 + 1) == p.rows;
-      const uint32_t stage = sQ + qb * kQBytes;
+      const bool valid = pl <= qls;
+      const int row0 = U.q_row0 + sub * p.rows;  // first q row of this query tile
+      const size_t orow = (size_t)(row0 + r / p.G) * p.Hq + h;
+      // A query tile whose rows all belong to its sequence is staged in its
+      // own Q buffer (the unit's last QK^T is done) in the 128-byte-swizzled
+      // layout of the output tensor map and written by one TMA store; a
+      // ragged tail tile stores its valid rows directly.
+      const bool full = (qls - q0s + 1) == p.rows;
+      const uint32_t stage = sQ + (qb * QT + sub) * kQBytes;
       uint16_t* op = reinterpret_cast<uint16_t*>(p.out) + orow * D;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {  // 64 columns per round trip
@@ -697,6 +750,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         for (int i = 0; i < 32; ++i)
           w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
         if (full) {
+          // 16-byte unit i of a 128-byte row sits at i ^ (row % 8) under the swizzle.
           const uint32_t row_addr = stage + c * kQChunk + (uint32_t)r * 128u;
 #pragma unroll
           for (int i = 0; i < 8; ++i)
@@ -711,13 +765,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
       }
       if (full) {
         fence_proxy_async_smem();  // generic-proxy writes -> visible to the TMA store
-        mbar_arrive(sBar + 8u * B::kEpi);
-        if (r == 0) {
-          if (!wait_bounded(sBar + 8u * B::kEpi, n_full & 1u, abort_flag, p.status, tmo)) {
+        mbar_arrive(bsub + 8u * B::kEpi);
+        if (leader) {
+          if (!wait_bounded(bsub + 8u * B::kEpi, n_full & 1u, abort_flag, p.status, tmo)) {
             ok = false;
           } else {
             for (int c = 0; c < NCH; ++c)
-              tma_store_3d(&p.tmap_o, stage + c * kQChunk, c * 64, U.g * p.G, U.q_row0);
+              tma_store_3d(&p.tmap_o, stage + c * kQChunk, c * 64, U.g * p.G, row0);
             bulk_commit_group();
           }
         }
@@ -726,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       if (valid && p.lse != nullptr) p.lse[orow] = lse2 * kLn2;
-      if (r == 0) {
+      if (leader) {
         if (NQ == 1) {
           bulk_wait_group_read0();
           mbar_arrive(sBar + 8u * (B::kQEmpty + qb));
@@ -735,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
           release_qb = qb;
         }
       }
-      if (p.unit_log != nullptr && r == 0) {
+      if (p.unit_log != nullptr && leader && sub == 0) {
         int32_t* rec = p.unit_log + 8 * (size_t)cur_u;
         rec[0] = U.b;
         rec[1] = U.g;
@@ -747,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         rec[7] = k;
       }
     }
-    if (r == 0) {
+    if (leader) {
       bulk_wait_group0();  // every output store complete before the CTA exits
       if (release_pending) mbar_arrive(sBar + 8u * (B::kQEmpty + release_qb));
     }
@@ -756,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
   // ---------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

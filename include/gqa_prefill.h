@@ -112,9 +112,11 @@ int gqa_flash_prefill(const void* q, const void* k, const void* v,
 
 /*
  * Launch plan of a call with these shapes (host only, no device access).
- * A work unit is (sequence, KV head, query tile): the kernel's 128-row MMA
- * tile packs the G query heads of one KV head over rows_per_unit query
- * positions (rows_per_unit * G = 128), and walks keys in tiles of block_n.
+ * A work unit is (sequence, KV head, query positions): the kernel's 128-row
+ * MMA tile packs the G query heads of one KV head over 128 / G query
+ * positions, a unit holds q_tiles such tiles (rows_per_unit = q_tiles * 128
+ * / G positions) that walk the same keys in tiles of block_n, so every K/V
+ * tile brought on chip serves q_tiles * 128 rows.
  */
 typedef struct {
     int rows_per_unit;  /* query positions per unit (128 / G) */
@@ -123,6 +125,7 @@ typedef struct {
     int ctas_per_sm;    /* resident CTAs per SM the launch assumes */
     int grid;           /* CTAs launched (persistent) */
     int max_units;      /* upper bound on units: Hkv * (ceil(total_q/rows) + B) */
+    int q_tiles;        /* 128-row query tiles per unit: 1, or 2 (one CTA per SM) */
 } gqa_prefill_plan_t;
 
 int gqa_prefill_plan(int num_seqs, int total_q, int max_seqlen_q, int Hq,
@@ -158,12 +161,25 @@ int gqa_flash_prefill_debug(const void* q, const void* k, const void* v,
 int gqa_prefill_force_block_n(int block_n);
 
 /*
+ * Force the number of 128-row query tiles per work unit for later calls in
+ * this process (0 restores the configuration cache's choice): 1, or 2 (two
+ * query tiles walk the same key tiles, so each K/V tile loaded serves 256
+ * rows; one CTA per SM with a deeper K/V ring).  2 exists for block_n 64 and
+ * 128 at d = 64 and block_n 64 at d = 128; a call whose shape has no such
+ * kernel returns GQA_ERR_UNSUPPORTED.  Returns GQA_OK or GQA_ERR_INVALID.
+ * Meant for tests and tuning.
+ */
+int gqa_prefill_force_q_tiles(int q_tiles);
+
+/*
  * Launch-configuration tuning.  The configuration cache is keyed on (d, a
  * power-of-two bucket of max_seqlen_q, Hq, G, windowed, dtype), never on the
  * KV length.  With tuning on (this call, or GQA_PREFILL_TUNE=1 in the
  * environment before the first call), the first call for an untuned key times
  * every candidate tile size on the caller's stream (without the sink) and
- * keeps the fastest; that call synchronises its stream, and tuning is skipped
+ * keeps the fastest (candidates: block_n 64, 96, 128 with one query tile per
+ * unit and 64, 128 with two, where the head dim has the kernel); that call
+ * synchronises its stream, and tuning is skipped
  * while the stream is being captured.  GQA_PREFILL_TUNE_DEBUG=1 prints the
  * timings.  enable: 0 or 1.  Returns GQA_OK or GQA_ERR_INVALID.
  */
@@ -173,12 +189,13 @@ int gqa_prefill_set_tuning(int enable);
 int gqa_prefill_clear_config_cache(void);
 
 /*
- * The cached tile size for a call with these shapes: *block_n = 0 if the key
- * has no entry yet; *tuned = 1 if the entry came from a timed sweep.
+ * The cached configuration for a call with these shapes: *block_n = 0 (and
+ * *q_tiles = 0) if the key has no entry yet; *tuned = 1 if the entry came
+ * from a timed sweep.  q_tiles may be NULL.
  */
 int gqa_prefill_config_block_n(int total_q, int max_seqlen_q, int Hq, int Hkv,
                                int d, int dtype, int window, int* block_n,
-                               int* tuned);
+                               int* q_tiles, int* tuned);
 
 /*
  * Failure-detection self-test: launches one thread that waits, through the

@@ -92,11 +92,11 @@ def test_empty_work_is_ok_without_launch(lib):
 def test_plan_is_host_only(lib):
     import gqa_flash_attention_prefill_gb300 as pkg
     p = pkg.plan(1, 4096, 4096, 64, 8, 64, "bf16", 0)
-    assert p["rows_per_unit"] == 16 and p["block_n"] in (64, 128)
-    assert p["max_units"] == 8 * (4096 // 16 + 1)
+    assert p["rows_per_unit"] == 16 * p["q_tiles"] and p["block_n"] in (64, 128)
+    assert p["max_units"] == 8 * (4096 // p["rows_per_unit"] + 1)
     assert p["grid"] >= 1
     p = pkg.plan(1, 256, 256, 4, 1, 64, "f16", 32)
-    assert p["rows_per_unit"] == 32
+    assert p["rows_per_unit"] == 32 * p["q_tiles"]
     with pytest.raises(pkg.GQAError):
         pkg.plan(1, 10, 10, 8, 2, 80, "bf16", 0)
 
@@ -105,6 +105,31 @@ def test_force_block_n_validates(lib):
     assert lib.gqa_prefill_force_block_n(80) == -1
     assert lib.gqa_prefill_force_block_n(64) == 0
     assert lib.gqa_prefill_force_block_n(0) == 0
+
+
+def test_force_q_tiles_validates_and_shapes_plan(lib):
+    import gqa_flash_attention_prefill_gb300 as pkg
+    for bad in (-1, 3, 4):
+        assert lib.gqa_prefill_force_q_tiles(bad) == -1
+    try:
+        pkg.force_q_tiles(2)
+        p = pkg.plan(1, 4096, 4096, 64, 8, 64, "bf16", 0)
+        assert p["q_tiles"] == 2 and p["rows_per_unit"] == 32
+        assert p["max_units"] == 8 * (4096 // 32 + 1)
+        assert p["ctas_per_sm"] == 1
+        pkg.force_block_n(96)  # no two-tile kernel for 96-key tiles: declined
+        with pytest.raises(pkg.GQAError):
+            pkg.plan(1, 4096, 4096, 64, 8, 64, "bf16", 0)
+        pkg.force_block_n(0)
+        with pytest.raises(pkg.GQAError):  # d = 256: two tiles exceed tensor memory
+            pkg.plan(1, 4096, 4096, 16, 2, 256, "bf16", 0)
+        pkg.force_q_tiles(1)
+        p = pkg.plan(1, 4096, 4096, 64, 8, 64, "bf16", 0)
+        assert p["q_tiles"] == 1 and p["rows_per_unit"] == 16
+    finally:
+        pkg.force_block_n(0)
+        pkg.force_q_tiles(0)
+    assert pkg.plan(1, 4096, 4096, 64, 8, 64, "bf16", 0)["q_tiles"] in (1, 2)
 
 
 def test_binding_refuses_to_run_without_library(tmp_path):

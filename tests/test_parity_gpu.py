@@ -20,6 +20,7 @@ def pkg():
     import gqa_flash_attention_prefill_gb300 as pkg
     pkg.load()
     pkg.force_block_n(0)
+    pkg.force_q_tiles(0)
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     return pkg
 
@@ -73,6 +74,47 @@ def test_block_n_variants(pkg, d, block_n, window):
         _check_full(pkg, b, label=f"d{d}/bn{block_n}/w{window}")
     finally:
         pkg.force_block_n(0)
+
+
+class _Variant:
+    """Pins the key-tile size and/or query tiles per unit for a block."""
+    def __init__(self, pkg, block_n=0, q_tiles=0):
+        self.pkg, self.bn, self.qt = pkg, block_n, q_tiles
+
+    def __enter__(self):
+        self.pkg.force_block_n(self.bn)
+        self.pkg.force_q_tiles(self.qt)
+
+    def __exit__(self, *exc):
+        self.pkg.force_block_n(0)
+        self.pkg.force_q_tiles(0)
+
+
+@pytest.mark.parametrize("d,block_n", [(64, 64), (64, 128), (128, 64)])
+@pytest.mark.parametrize("window", [0, 1, 15, 100, 129])
+@pytest.mark.parametrize("sink_mode,dtype", [("head", "bf16"), ("smooth", "f16"), ("none", "bf16")])
+def test_two_query_tiles_per_unit(pkg, d, block_n, window, sink_mode, dtype):
+    """Two 128-row query tiles walking the same key tiles: ragged sequences
+    whose last unit has a partial or an empty second tile."""
+    b = W.make_batch([0, 190, 3, 1000], [300, 257, 129, 17], 16, 2, d, dtype, window=window,
+                     sink_mode=sink_mode, seed=5 * d + block_n + window)
+    with _Variant(pkg, block_n, 2):
+        _check_full(pkg, b, label=f"2 tiles d{d}/bn{block_n}/w{window}/{sink_mode}")
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 2), (64, 8), (128, 1), (16, 16)])
+def test_two_query_tiles_group_sizes(pkg, hq, hkv):
+    b = W.make_batch([3, 130, 0], [70, 300, 1], hq, hkv, 64, "bf16", window=33,
+                     sink_mode="head", seed=hq * 37 + hkv)
+    with _Variant(pkg, 0, 2):
+        _check_full(pkg, b)
+
+
+@pytest.mark.parametrize("q_tiles", [1, 2])
+def test_layer_pair_small_both_unit_sizes(pkg, q_tiles):
+    with _Variant(pkg, 0, q_tiles):
+        for b in W.layer_pair(seq=640, seed=4):
+            _check_full(pkg, b, label=f"{b.name}/{q_tiles} tiles")
 
 
 def test_layer_pair_small_full_output(pkg):
@@ -159,11 +201,13 @@ def _bookkeeping(pkg, batch):
     return p, used
 
 
+@pytest.mark.parametrize("q_tiles", [1, 2])
 @pytest.mark.parametrize("window", [0, 1, 15, 100, 128, 129, 4096])
-def test_bookkeeping_bit_exact_ragged(pkg, window):
+def test_bookkeeping_bit_exact_ragged(pkg, window, q_tiles):
     b = W.make_batch([0, 37, 5000, 129, 64], [1, 300, 700, 128, 129], 64, 8, 64, "bf16",
                      window=window, sink_mode="head", seed=window + 1)
-    _bookkeeping(pkg, b)
+    with _Variant(pkg, 0, q_tiles):
+        _bookkeeping(pkg, b)
 
 
 def test_bookkeeping_full_size_layer_pair(pkg):
@@ -243,9 +287,10 @@ def test_ragged_full_size_sampled(pkg, hq, hkv, d, window, sink, dtype):
 
 # ------------------------------------------------------------- exact key sets
 
+@pytest.mark.parametrize("q_tiles", [1, 2])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("window", [0, 1, 15, 64, 100, 129])
-def test_counting_probe_exact_key_sets(pkg, dtype, window):
+def test_counting_probe_exact_key_sets(pkg, dtype, window, q_tiles):
     """q = 0 makes every kept probability exactly 1, so lse = ln(n) and, with
     v[j, c] = [j mod 64 == c], out[c] * n counts the kept keys in each residue
     class: integers recovered exactly pin every row's key set."""
@@ -256,7 +301,8 @@ def test_counting_probe_exact_key_sets(pkg, dtype, window):
         b.kv_indptr[:-1], torch.diff(b.kv_indptr))
     b.v.zero_()
     b.v[torch.arange(b.total_kv), :, j % 64] = 1.0
-    out, lse = run_gpu(pkg, b)
+    with _Variant(pkg, 0, q_tiles):
+        out, lse = run_gpu(pkg, b)
     n = torch.exp(lse.double()).round().long()
     counts = (out.double() * n[..., None]).round().long()
     cu, pre = b.cu_seqlens_q.tolist(), b.prefix_lens.tolist()

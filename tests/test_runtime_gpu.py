@@ -16,6 +16,7 @@ def pkg():
     import gqa_flash_attention_prefill_gb300 as pkg
     pkg.load()
     pkg.force_block_n(0)
+    pkg.force_q_tiles(0)
     return pkg
 
 
@@ -34,16 +35,17 @@ def test_tuning_sweep_fills_the_cache(pkg):
     pkg.set_tuning(True)
     try:
         b = W.make_batch([0], [1024], 64, 8, 64, "bf16", window=0, sink_mode="head", seed=8)
-        assert pkg.config_block_n(b.total_q, b.max_seqlen_q, 64, 8, 64, "bf16", 0) == (0, False)
+        assert pkg.config_block_n(b.total_q, b.max_seqlen_q, 64, 8, 64, "bf16", 0) == (0, 0, False)
         out, lse = run_gpu(pkg, b)
-        bn, tuned = pkg.config_block_n(b.total_q, b.max_seqlen_q, 64, 8, 64, "bf16", 0)
-        assert tuned and bn in (64, 128)
+        bn, qt, tuned = pkg.config_block_n(b.total_q, b.max_seqlen_q, 64, 8, 64, "bf16", 0)
+        assert tuned and bn in (64, 96, 128) and qt in (1, 2)
         ref, ref_lse = run_oracle(b, rows=list(range(0, 1024, 37)))
         rows = list(range(0, 1024, 37))
         compare(out, lse, ref, ref_lse, rows=rows, label="tuned")
         # the key ignores the KV length: a longer prefix reuses the entry
         b2 = W.make_batch([3000], [1000], 64, 8, 64, "bf16", window=0, sink_mode="head", seed=9)
-        assert pkg.config_block_n(b2.total_q, b2.max_seqlen_q, 64, 8, 64, "bf16", 0) == (bn, True)
+        assert pkg.config_block_n(b2.total_q, b2.max_seqlen_q, 64, 8, 64, "bf16", 0) == \
+            (bn, qt, True)
     finally:
         pkg.set_tuning(False)
         pkg.clear_config_cache()
