@@ -338,21 +338,24 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
   const uint32_t tmem = misc[0];
 
   // ---------------------------------------------------------------- producer
-  // Two iterators over the CTA's sequence of key tiles: K runs up to one tile
-  // ahead of V (a K slot frees when its QK^T is done, a V slot only when its
-  // PV is done), and a unit's Q tiles are requested just before its first K.
-  // With a single Q buffer the V iterator first finishes the previous unit,
-  // whose epilogue must release that buffer.
+  // Two lanes of the producer warp, each with its own bounded waits: lane 0
+  // walks the CTA's key tiles loading each unit's Q tiles and then its K
+  // tiles, lane 1 walks the same tiles loading V.  K therefore runs as far
+  // ahead as its ring allows (a K slot frees when its QK^T is done), however
+  // late a V slot frees (when its PV is done).
   if (warp == kProdWarp) {
     if (lane == 0) {
-      uint32_t nq = 0, nk[NS], nv[NS];
-      for (int s = 0; s < NS; ++s) nk[s] = nv[s] = 0u;
-      bool ok = true;
-      auto issue_q = [&](const Unit& U) -> bool {
+      uint32_t nq = 0, nk[NS];
+      for (int s = 0; s < NS; ++s) nk[s] = 0u;
+      uint32_t itk = 0;
+      for (int kk = 0;; ++kk) {
+        const int uk = unit_of(kk);
+        if (uk >= n_units) break;
+        const Unit U = decode_unit(p, T, uk, BN, urows);
         const uint32_t qb = nq % NQ;
         if (!wait_bounded(sBar + 8u * (B::kQEmpty + qb), ((nq / NQ) & 1u) ^ 1u, abort_flag,
                           p.status, tmo))
-          return false;
+          break;
         mbar_arrive_expect_tx(sBar + 8u * (B::kQFull + qb), QT * kQBytes);
         // A query tile past the end of q (a unit's second tile at the end of
         // the batch) reads the tensor map's zero fill; its rows are never stored.
@@ -361,52 +364,19 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
             tma_load_3d(sQ + (qb * QT + t) * kQBytes + c * kQChunk, &p.tmap_q,
                         sBar + 8u * (B::kQFull + qb), c * 64, U.g * p.G, U.q_row0 + t * p.rows);
         ++nq;
-        return true;
-      };
-      int kk = 0, jk = 0, uk = unit_of(0);
-      uint32_t itk = 0;
-      Unit Uk;
-      if (uk < n_units) Uk = decode_unit(p, T, uk, BN, urows);
-      int kv = 0, jv = 0, uv = uk;
-      uint32_t itv = 0;
-      Unit Uv = Uk;
-      while (ok && uv < n_units) {
-        bool do_k = (uk < n_units) && itk <= itv + 1u;
-        if (do_k && NQ == 1 && jk == 0 && itv < itk) do_k = false;
-        if (do_k) {
-          if (jk == 0 && !(ok = issue_q(Uk))) break;
+        bool ok = true;
+        for (int j = 0; j < U.n_tiles; ++j, ++itk) {
           const uint32_t s = itk % NS, ph = (itk / NS) & 1u;
           if (!(ok = wait_bounded(sBar + 8u * (B::kKEmpty + s), ph ^ 1u, abort_flag, p.status, tmo)))
             break;
           mbar_arrive_expect_tx(sBar + 8u * (B::kKFull + s), kKVBytes);
-          const int row = Uk.kv_base + Uk.kv_lo + jk * BN;
+          const int row = U.kv_base + U.kv_lo + j * BN;
           for (int c = 0; c < NCH; ++c)
             tma_load_3d(sK + s * kKVBytes + c * kKVChunk, &p.tmap_k, sBar + 8u * (B::kKFull + s),
-                        c * 64, Uk.g, row);
+                        c * 64, U.g, row);
           ++nk[s];
-          ++itk;
-          if (++jk == Uk.n_tiles) {
-            jk = 0;
-            uk = unit_of(++kk);
-            if (uk < n_units) Uk = decode_unit(p, T, uk, BN, urows);
-          }
-        } else {
-          const uint32_t s = itv % NS, ph = (itv / NS) & 1u;
-          if (!(ok = wait_bounded(sBar + 8u * (B::kVEmpty + s), ph ^ 1u, abort_flag, p.status, tmo)))
-            break;
-          mbar_arrive_expect_tx(sBar + 8u * (B::kVFull + s), kKVBytes);
-          const int row = Uv.kv_base + Uv.kv_lo + jv * BN;
-          for (int c = 0; c < NCH; ++c)
-            tma_load_3d(sV + s * kKVBytes + c * kKVChunk, &p.tmap_v, sBar + 8u * (B::kVFull + s),
-                        c * 64, Uv.g, row);
-          ++nv[s];
-          ++itv;
-          if (++jv == Uv.n_tiles) {
-            jv = 0;
-            uv = unit_of(++kv);
-            if (uv < n_units) Uv = decode_unit(p, T, uv, BN, urows);
-          }
         }
+        if (!ok) break;
       }
       // Let every copy issued land before the CTA can exit.
       for (uint32_t b = 0; b < NQ; ++b) {
@@ -415,10 +385,31 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
           wait_drain(sBar + 8u * (B::kQFull + last % NQ), (last / NQ) & 1u, tmo);
         }
       }
-      for (int s = 0; s < NS; ++s) {
+      for (int s = 0; s < NS; ++s)
         if (nk[s] > 0) wait_drain(sBar + 8u * (B::kKFull + s), (nk[s] - 1u) & 1u, tmo);
-        if (nv[s] > 0) wait_drain(sBar + 8u * (B::kVFull + s), (nv[s] - 1u) & 1u, tmo);
+    } else if (lane == 1) {
+      uint32_t nv[NS];
+      for (int s = 0; s < NS; ++s) nv[s] = 0u;
+      uint32_t itv = 0;
+      bool ok = true;
+      for (int kv = 0; ok; ++kv) {
+        const int uv = unit_of(kv);
+        if (uv >= n_units) break;
+        const Unit U = decode_unit(p, T, uv, BN, urows);
+        for (int j = 0; j < U.n_tiles; ++j, ++itv) {
+          const uint32_t s = itv % NS, ph = (itv / NS) & 1u;
+          if (!(ok = wait_bounded(sBar + 8u * (B::kVEmpty + s), ph ^ 1u, abort_flag, p.status, tmo)))
+            break;
+          mbar_arrive_expect_tx(sBar + 8u * (B::kVFull + s), kKVBytes);
+          const int row = U.kv_base + U.kv_lo + j * BN;
+          for (int c = 0; c < NCH; ++c)
+            tma_load_3d(sV + s * kKVBytes + c * kKVChunk, &p.tmap_v, sBar + 8u * (B::kVFull + s),
+                        c * 64, U.g, row);
+          ++nv[s];
+        }
       }
+      for (int s = 0; s < NS; ++s)
+        if (nv[s] > 0) wait_drain(sBar + 8u * (B::kVFull + s), (nv[s] - 1u) & 1u, tmo);
     }
     __syncwarp();
   }
