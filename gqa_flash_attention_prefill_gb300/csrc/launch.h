@@ -3,9 +3,13 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "prefill_kernel.cuh"
 
 namespace gqa {
+
+constexpr int kMaxDevices = 64;
 
 struct KernelShape {
   int block_n;      // keys per tile
@@ -32,12 +36,26 @@ cudaError_t launch_d128(const PrefillParams& p, const KernelShape& ks, bool win,
 cudaError_t launch_d256(const PrefillParams& p, const KernelShape& ks, bool win, bool bf16,
                         int grid, unsigned smem, cudaStream_t st);
 
+// Largest dynamic shared memory already allowed for one kernel on each device,
+// so that the attribute is set once rather than on every launch.
+struct SmemAttr {
+  std::atomic<unsigned> allowed[kMaxDevices];
+};
+
 template <int D, int BN, int NS, bool WIN, bool BF16, int MINB, int QT>
 cudaError_t launch_one(const PrefillParams& p, int grid, unsigned smem, cudaStream_t st) {
   auto kern = prefill_kernel<D, BN, NS, WIN, BF16, MINB, QT>;
+  static SmemAttr attr{};
   if (smem < smem_bytes_for(D, BN, NS, QT)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (attr.allowed[dev].load(std::memory_order_acquire) < smem) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr.allowed[dev].store(smem, std::memory_order_release);
+  }
   kern<<<grid, threads_for(QT), smem, st>>>(p);
   return cudaGetLastError();
 }
