@@ -352,6 +352,13 @@ def run_workload(args, rank, world):
         desc = ("ragged varlen: 16 sequences, prefixes U[0,16384], extends U[1,8192], 64/8, d 64, "
                 "bf16, window 128, sinks")
         tokens = b.total_q
+    elif args.workload == "short_chunk":
+        calls = [W.make_batch([16384, 16384], [64, 64], 64, 8, 64, "bf16", window=w,
+                              sink_mode="head", seed=5 + i, name=f"short-chunk-w{w}").to(dev)
+                 for i, w in enumerate((0, 128))]
+        desc = ("short chunks over long prefixes: 2 sequences x (prefix 16384 + extend 64), "
+                "64/8, d 64, bf16, sinks; one full-causal and one window-128 call per step")
+        tokens = 2 * 128
     else:
         raise ValueError(args.workload)
     flops = 0.0
@@ -362,10 +369,23 @@ def run_workload(args, rank, world):
     lses = [torch.empty(b.q.shape[:2], dtype=torch.float32, device=dev) for b in calls]
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    # --splits >= 0: the split-KV entry point (0 = the library's choice), with a
+    # workspace per call allocated here, outside the timed region.
+    splits_used, workspaces = [], []
+    if args.splits >= 0:
+        for b in calls:
+            used, nbytes = pkg.splitkv_workspace(b.num_seqs, b.total_q, b.max_seqlen_q, b.hq,
+                                                 b.hkv, b.d, b.dtype_name, b.window, args.splits)
+            splits_used.append(used)
+            workspaces.append(torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev))
 
     def step():
-        for b, o, l in zip(calls, outs, lses):
-            pkg.prefill(b, out=o, lse=l, stream=stream)
+        for i, (b, o, l) in enumerate(zip(calls, outs, lses)):
+            if args.splits >= 0:
+                pkg.prefill_splitkv(b, num_splits=args.splits, workspace=workspaces[i], out=o,
+                                    lse=l, stream=stream)
+            else:
+                pkg.prefill(b, out=o, lse=l, stream=stream)
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
@@ -394,10 +414,13 @@ def run_workload(args, rank, world):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) Q/K/V and sinks; no model weights)",
             "config": {"workload": desc, "l2": "flushed between steps (256 MiB write)",
-                       "calls_per_step": len(calls)},
+                       "calls_per_step": len(calls),
+                       "entry": ("gqa_flash_prefill_splitkv, splits " + str(splits_used))
+                       if args.splits >= 0 else "gqa_flash_prefill"},
             "tokens_per_s": round(world * tokens / (ms_step * 1e-3), 1),
             "pct_of_bf16_peak": round(100.0 * value / (world * peaks["bf16_tflops"]), 2),
-            "gpu_launches": len(calls) * args.steps, "clocks": clk.summary()}
+            "gpu_launches": len(calls) * args.steps + sum(1 for s_ in splits_used if s_ > 1) * args.steps,
+            "clocks": clk.summary()}
     if args.workload == "chunked_prefix":
         # HBM-bound: Q read and O (+ lse) written once; of K and V only the rows some
         # window reaches (the window-bounded layout's rows) must be read, in either layout.
@@ -519,11 +542,14 @@ def main():
                     help="CPU work of the oracle baseline sample (rank 0, N=1)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="layer_pair",
-                    choices=["layer_pair", "chunked_prefix", "oss20b_16k", "ragged"],
+                    choices=["layer_pair", "chunked_prefix", "oss20b_16k", "ragged", "short_chunk"],
                     help="layer_pair is the headline configuration; the others are "
                          "supplementary measurements")
     ap.add_argument("--layout", default="window-bounded", choices=["window-bounded", "full-prefix"],
                     help="KV layout of the chunked_prefix workload")
+    ap.add_argument("--splits", type=int, default=-1,
+                    help="supplementary workloads: -1 the plain entry point; 0 split-KV with "
+                         "the library's split count; k >= 1 split-KV with k splits")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

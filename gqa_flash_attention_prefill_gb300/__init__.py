@@ -14,6 +14,7 @@ from typing import Optional
 
 __all__ = ["load", "gqa_flash_prefill", "gqa_flash_prefill_debug", "prefill",
            "plan", "force_block_n", "force_q_tiles", "get_device_status", "set_tuning",
+           "gqa_flash_prefill_splitkv", "splitkv_workspace", "prefill_splitkv",
            "clear_config_cache", "config_block_n", "selftest_timeout", "GQAError",
            "GQA_F16", "GQA_BF16", "GQA_DEV_TIMEOUT", "GQA_DEV_BAD_METADATA",
            "EXPORTED_SYMBOLS"]
@@ -28,6 +29,7 @@ EXPORTED_SYMBOLS = [
     "gqa_prefill_status_string", "gqa_prefill_version", "gqa_prefill_set_tuning",
     "gqa_prefill_clear_config_cache", "gqa_prefill_config_block_n",
     "gqa_prefill_selftest_timeout", "gqa_prefill_force_q_tiles",
+    "gqa_flash_prefill_splitkv", "gqa_prefill_splitkv_workspace",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -68,6 +70,11 @@ def load(path: Optional[str] = None):
     lib.gqa_flash_prefill.restype = ctypes.c_int
     lib.gqa_flash_prefill_debug.argtypes = core + [vp]
     lib.gqa_flash_prefill_debug.restype = ctypes.c_int
+    lib.gqa_flash_prefill_splitkv.argtypes = core[:-1] + [ctypes.c_int, vp, ctypes.c_size_t, vp]
+    lib.gqa_flash_prefill_splitkv.restype = ctypes.c_int
+    lib.gqa_prefill_splitkv_workspace.argtypes = [ctypes.c_int] * 9 + [
+        ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_size_t)]
+    lib.gqa_prefill_splitkv_workspace.restype = ctypes.c_int
     lib.gqa_prefill_plan.argtypes = [ctypes.c_int] * 8 + [ctypes.POINTER(_Plan)]
     lib.gqa_prefill_plan.restype = ctypes.c_int
     lib.gqa_prefill_force_block_n.argtypes = [ctypes.c_int]
@@ -167,6 +174,59 @@ def gqa_flash_prefill_debug(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, scale
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_flash_prefill_debug")
     return out
+
+
+def gqa_flash_prefill_splitkv(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, scale,
+                              workspace, num_splits=0, window=0, sinks=None,
+                              smooth_softmax=False, out=None, lse=None, stream=None,
+                              max_seqlen_q=0):
+    """Split-KV form of gqa_flash_prefill (see gqa_prefill.h); ``workspace``
+    is a device tensor (any dtype) at least ``splitkv_workspace(...)`` bytes,
+    or None when the call does not split."""
+    a = _args(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, scale, window, sinks,
+              smooth_softmax, out, lse, stream, max_seqlen_q)
+    ws = _ptr(workspace)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().gqa_flash_prefill_splitkv(*a[:-1], int(num_splits), ws, nbytes, a[-1])
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_flash_prefill_splitkv")
+    return out
+
+
+def splitkv_workspace(num_seqs, total_q, max_seqlen_q, hq, hkv, d, dtype, window,
+                      num_splits=0):
+    """(splits used, workspace bytes) for a split-KV call with these shapes."""
+    used, nbytes = ctypes.c_int(0), ctypes.c_size_t(0)
+    code = dtype if isinstance(dtype, int) else (GQA_BF16 if "bf16" in str(dtype) else GQA_F16)
+    rc = load().gqa_prefill_splitkv_workspace(int(num_seqs), int(total_q), int(max_seqlen_q),
+                                              int(hq), int(hkv), int(d), code, int(window),
+                                              int(num_splits), ctypes.byref(used),
+                                              ctypes.byref(nbytes))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_prefill_splitkv_workspace")
+    return used.value, nbytes.value
+
+
+def prefill_splitkv(batch, num_splits=0, workspace=None, out=None, lse=None, with_lse=True,
+                    stream=None):
+    """Split-KV run of one ``workloads.Batch`` already on the GPU; allocates the
+    workspace (and out/lse) with torch when not given.  Returns (out, lse)."""
+    import torch
+    if out is None:
+        out = torch.empty_like(batch.q)
+    if lse is None and with_lse:
+        lse = torch.empty(batch.q.shape[:2], dtype=torch.float32, device=batch.q.device)
+    used, nbytes = splitkv_workspace(batch.num_seqs, batch.total_q, batch.max_seqlen_q,
+                                     batch.hq, batch.hkv, batch.d, batch.dtype_name,
+                                     batch.window, num_splits)
+    if workspace is None and nbytes > 0:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=batch.q.device)
+    gqa_flash_prefill_splitkv(batch.q, batch.k, batch.v, batch.cu_seqlens_q,
+                              batch.prefix_lens, batch.kv_indptr, batch.scale, workspace,
+                              num_splits=num_splits, window=batch.window, sinks=batch.sinks,
+                              smooth_softmax=batch.smooth, out=out, lse=lse, stream=stream,
+                              max_seqlen_q=batch.max_seqlen_q)
+    return out, lse
 
 
 def prefill(batch, out=None, lse=None, with_lse=True, stream=None):

@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgqa_prefill.so")
-SOURCES = ["host.cu", "inst_d64.cu", "inst_d64_pair.cu", "inst_d128.cu", "inst_d256.cu"]
+SOURCES = ["host.cu", "inst_d64.cu", "inst_d64_pair.cu", "inst_d128.cu", "inst_d256.cu",
+           "inst_split.cu", "merge.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -28,8 +29,9 @@ def nvcc() -> str:
 
 
 def _flags():
+    # Hidden by default: the library exports only the C ABI (GQA_API).
     return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-                   "-I", CSRC, "-I", INCLUDE]
+                   "-Xcompiler", "-fvisibility=hidden", "-I", CSRC, "-I", INCLUDE]
 
 
 def _deps_mtime() -> float:

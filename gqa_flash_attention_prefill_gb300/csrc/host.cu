@@ -146,8 +146,54 @@ struct Plan {
   int rows;       // query positions per 128-row query tile (128 / G)
   int unit_rows;  // query positions per unit (q_tiles * rows)
   int G, ctas_per_sm, grid, max_units;
+  int slots;      // CTAs resident at once (SMs x CTAs per SM)
   unsigned smem_launch;  // dynamic smem requested per CTA
 };
+
+// Split-KV: S splits per unit; partials live in a caller-provided workspace.
+struct SplitArgs {
+  int num_splits = 1;
+  float* part_o = nullptr;
+  float* part_ml = nullptr;
+  int32_t* part_hdr = nullptr;
+};
+constexpr int kMaxSplits = 16;
+
+struct SplitLayout {
+  size_t o_off, ml_off, hdr_off, bytes;
+};
+// Workspace layout for S splits: partial O (fp32, d per row), (m, l) per row,
+// and the unit headers, each 256-byte aligned.
+SplitLayout split_layout(const Plan& pl, int d, int S) {
+  auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t items = (size_t)pl.max_units * S;
+  const size_t rows = (size_t)pl.shape.q_tiles * 128;
+  SplitLayout L;
+  L.o_off = 0;
+  L.ml_off = al(items * rows * (size_t)d * 4u);
+  L.hdr_off = L.ml_off + al(items * rows * 8u);
+  L.bytes = L.hdr_off + al((4u + 4u * (size_t)pl.max_units) * 4u);
+  return L;
+}
+
+// Split count when the caller leaves it to the library: only when the units
+// fill less than half of the resident CTAs, the S in [2, 16] that minimises
+// the waves of work items per split (ceil(units S / slots) / S) plus a small
+// per-split cost for the partials and the merge.
+int choose_splits(int units, int slots) {
+  if (units <= 0 || 2 * units >= slots) return 1;
+  int best = 1;
+  double best_cost = 1.0;
+  for (int S = 2; S <= kMaxSplits; ++S) {
+    const double waves = std::ceil((double)units * S / slots);
+    const double cost = waves / S + 0.01 * S;
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = S;
+    }
+  }
+  return best;
+}
 
 CfgKey cfg_key(int d, int total_q, int max_seqlen_q, int Hq, int G, int window, int dtype) {
   return CfgKey{d, pow2_bucket(max_seqlen_q > 0 ? max_seqlen_q : total_q), Hq, G,
@@ -214,6 +260,7 @@ int make_plan_bn(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, i
     if (pad > pl->smem_launch) pl->smem_launch = pad;
   }
   const int sms = have_dev ? di.sms : 152;
+  pl->slots = sms * cps;
   long long grid = (long long)sms * cps;
   if (grid > max_units) grid = max_units;
   if (grid < 1) grid = 1;
@@ -291,7 +338,8 @@ int launch_planned(const Plan& pl, const void* q, const void* k, const void* v,
                    const int32_t* cu_seqlens_q, const int32_t* prefix_lens,
                    const int32_t* kv_indptr, int num_seqs, int total_q, int total_kv, int Hq,
                    int Hkv, int d, int dtype, float scale, int window, const float* sinks,
-                   int smooth_softmax, void* out, float* lse, void* stream, int32_t* unit_log) {
+                   int smooth_softmax, void* out, float* lse, void* stream, int32_t* unit_log,
+                   const SplitArgs& sp = SplitArgs()) {
   DeviceInfo di;
   if (device_info(&di) != GQA_OK) return GQA_ERR_CUDA;
 
@@ -321,23 +369,36 @@ int launch_planned(const Plan& pl, const void* q, const void* k, const void* v,
   p.smooth = smooth_softmax != 0 ? 1 : 0;
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.timeout_ns = timeout_ns();
+  p.num_splits = sp.num_splits > 1 ? sp.num_splits : 1;
+  p.part_o = sp.part_o;
+  p.part_ml = sp.part_ml;
+  p.part_hdr = sp.part_hdr;
+  int grid = pl.grid;
+  if (p.num_splits > 1) {  // more work items than units: fill the resident slots
+    const long long items = (long long)pl.max_units * p.num_splits;
+    grid = (int)(items < pl.slots ? items : pl.slots);
+  }
   const bool win = p.window > 0;
   const bool bf16 = dtype == GQA_BF16;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (d == 64)
-    e = launch_d64(p, pl.shape, win, bf16, pl.grid, pl.smem_launch, st);
+  if (p.num_splits > 1)
+    e = launch_split(p, pl.shape, d, win, bf16, grid, pl.smem_launch, st);
+  else if (d == 64)
+    e = launch_d64(p, pl.shape, win, bf16, grid, pl.smem_launch, st);
   else if (d == 128)
-    e = launch_d128(p, pl.shape, win, bf16, pl.grid, pl.smem_launch, st);
+    e = launch_d128(p, pl.shape, win, bf16, grid, pl.smem_launch, st);
   else
-    e = launch_d256(p, pl.shape, win, bf16, pl.grid, pl.smem_launch, st);
+    e = launch_d256(p, pl.shape, win, bf16, grid, pl.smem_launch, st);
+  if (e == cudaSuccess && p.num_splits > 1)
+    e = launch_merge(p, d, bf16, pl.shape.q_tiles * 128, pl.max_units, st);
   if (debug_flag())
     std::fprintf(stderr,
                  "[gqa_prefill] B=%d total_q=%d total_kv=%d Hq=%d Hkv=%d d=%d %s window=%d "
                  "sink=%s block_n=%d q_tiles=%d stages=%d grid=%d (%d/SM) max_units=%d -> %s\n",
                  num_seqs, total_q, total_kv, Hq, Hkv, d, bf16 ? "bf16" : "f16", p.window,
                  sinks ? "head" : (p.smooth ? "smooth" : "none"), pl.shape.block_n,
-                 pl.shape.q_tiles, pl.shape.kv_stages, pl.grid, pl.ctas_per_sm, pl.max_units,
+                 pl.shape.q_tiles, pl.shape.kv_stages, grid, pl.ctas_per_sm, pl.max_units,
                  e == cudaSuccess ? "launched" : cudaGetErrorString(e));
   return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
@@ -417,11 +478,37 @@ int tune_key(const void* q, const void* k, const void* v, const int32_t* cu_seql
   return GQA_OK;
 }
 
+// Split count for a plan: `req` 0 = the library's choice, else 1..kMaxSplits.
+int splits_for(const Plan& pl, int total_q, int Hkv, int req) {
+  if (req != 0) return req;
+  const long long units = (long long)Hkv * ((total_q + pl.unit_rows - 1) / pl.unit_rows);
+  return choose_splits(units > (1ll << 30) ? (1 << 30) : (int)units, pl.slots);
+}
+
+// The plan of a split-KV call: the cached or forced plan when a split
+// instantiation exists for its shape, else one query tile per unit with the
+// key tile the split instantiations have for d.
+int plan_split(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, int d, int dtype,
+               int window, int req, Plan* pl, int* S) {
+  int rc = make_plan(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, pl);
+  if (rc != GQA_OK) return rc;
+  *S = splits_for(*pl, total_q, Hkv, req);
+  if (*S > 1 && !split_shape(d, pl->shape.block_n, pl->shape.q_tiles)) {
+    const int bn = split_shape(d, pl->shape.block_n, 1) ? pl->shape.block_n : (d == 64 ? 128 : 64);
+    rc = make_plan_bn(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, bn, 1, pl);
+    if (rc != GQA_OK) return rc;
+    *S = splits_for(*pl, total_q, Hkv, req);
+  }
+  return GQA_OK;
+}
+
 int run(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
         const int32_t* prefix_lens, const int32_t* kv_indptr, int num_seqs, int total_q,
         int total_kv, int max_seqlen_q, int Hq, int Hkv, int d, int dtype, float scale,
         int window, const float* sinks, int smooth_softmax, void* out, float* lse, void* stream,
-        int32_t* unit_log) {
+        int32_t* unit_log, int num_splits = 1, void* workspace = nullptr,
+        size_t workspace_bytes = 0) {
+  if (num_splits < 0 || num_splits > kMaxSplits) return GQA_ERR_INVALID;
   if (num_seqs < 0 || total_q < 0 || total_kv < 0 || max_seqlen_q < 0) return GQA_ERR_INVALID;
   if (Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return GQA_ERR_INVALID;
   if (dtype != GQA_F16 && dtype != GQA_BF16) return GQA_ERR_INVALID;
@@ -451,11 +538,25 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q
     }
   }
   Plan pl;
-  const int rc = make_plan(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, &pl);
+  SplitArgs sp;
+  const int rc = (num_splits == 1)
+                     ? make_plan(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, &pl)
+                     : plan_split(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window,
+                                  num_splits, &pl, &sp.num_splits);
   if (rc != GQA_OK) return rc;
+  if (sp.num_splits > 1) {
+    const SplitLayout L = split_layout(pl, d, sp.num_splits);
+    if (workspace == nullptr || workspace_bytes < L.bytes ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+      return GQA_ERR_INVALID;
+    char* base = static_cast<char*>(workspace);
+    sp.part_o = reinterpret_cast<float*>(base + L.o_off);
+    sp.part_ml = reinterpret_cast<float*>(base + L.ml_off);
+    sp.part_hdr = reinterpret_cast<int32_t*>(base + L.hdr_off);
+  }
   return launch_planned(pl, q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs, total_q,
                         total_kv, Hq, Hkv, d, dtype, scale, window, sinks, smooth_softmax, out, lse,
-                        stream, unit_log);
+                        stream, unit_log, sp);
 }
 
 }  // namespace
@@ -511,6 +612,33 @@ int gqa_flash_prefill_debug(const void* q, const void* k, const void* v,
   return gqa::run(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs, total_q, total_kv,
                   max_seqlen_q, Hq, Hkv, d, dtype, scale, window, sinks, smooth_softmax, out, lse,
                   stream, unit_log);
+}
+
+int gqa_flash_prefill_splitkv(const void* q, const void* k, const void* v,
+                              const int32_t* cu_seqlens_q, const int32_t* prefix_lens,
+                              const int32_t* kv_indptr, int num_seqs, int total_q, int total_kv,
+                              int max_seqlen_q, int Hq, int Hkv, int d, int dtype, float scale,
+                              int window, const float* sinks, int smooth_softmax, void* out,
+                              float* lse, int num_splits, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  return gqa::run(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs, total_q, total_kv,
+                  max_seqlen_q, Hq, Hkv, d, dtype, scale, window, sinks, smooth_softmax, out, lse,
+                  stream, nullptr, num_splits, workspace, workspace_bytes);
+}
+
+int gqa_prefill_splitkv_workspace(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv,
+                                  int d, int dtype, int window, int num_splits, int* splits_used,
+                                  size_t* bytes) {
+  if (splits_used == nullptr || bytes == nullptr) return GQA_ERR_INVALID;
+  if (num_splits < 0 || num_splits > gqa::kMaxSplits) return GQA_ERR_INVALID;
+  gqa::Plan pl;
+  int S = 1;
+  const int rc = gqa::plan_split(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window,
+                                 num_splits, &pl, &S);
+  if (rc != GQA_OK) return rc;
+  *splits_used = S;
+  *bytes = S > 1 ? gqa::split_layout(pl, d, S).bytes : 0;
+  return GQA_OK;
 }
 
 int gqa_prefill_plan(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, int d,

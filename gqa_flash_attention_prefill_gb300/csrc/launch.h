@@ -35,6 +35,21 @@ cudaError_t launch_d128(const PrefillParams& p, const KernelShape& ks, bool win,
                         int grid, unsigned smem, cudaStream_t st);
 cudaError_t launch_d256(const PrefillParams& p, const KernelShape& ks, bool win, bool bf16,
                         int grid, unsigned smem, cudaStream_t st);
+// Split-KV instantiations (inst_split.cu); false from split_shape when (d,
+// block_n, q_tiles) has none.
+bool split_shape(int d, int block_n, int q_tiles);
+cudaError_t launch_split(const PrefillParams& p, const KernelShape& ks, int d, bool win,
+                         bool bf16, int grid, unsigned smem, cudaStream_t st);
+
+// Split-KV merge (merge.cu): one 128-thread block per unit, `grid` >= units.
+cudaError_t launch_merge(const PrefillParams& p, int d, bool bf16, int part_rows, int grid,
+                         cudaStream_t st);
+
+// The launch helpers have internal linkage (one copy per translation unit):
+// a function-local static in a template with external linkage is merged
+// across shared objects by the dynamic linker, so two loaded copies of this
+// library would share the cache below while owning different kernels.
+namespace {
 
 // Largest dynamic shared memory already allowed for one kernel on each device,
 // so that the attribute is set once rather than on every launch.
@@ -42,9 +57,9 @@ struct SmemAttr {
   std::atomic<unsigned> allowed[kMaxDevices];
 };
 
-template <int D, int BN, int NS, bool WIN, bool BF16, int MINB, int QT>
+template <int D, int BN, int NS, bool WIN, bool BF16, int MINB, int QT, bool SPL>
 cudaError_t launch_one(const PrefillParams& p, int grid, unsigned smem, cudaStream_t st) {
-  auto kern = prefill_kernel<D, BN, NS, WIN, BF16, MINB, QT>;
+  auto kern = prefill_kernel<D, BN, NS, WIN, BF16, MINB, QT, SPL>;
   static SmemAttr attr{};
   if (smem < smem_bytes_for(D, BN, NS, QT)) return cudaErrorInvalidValue;
   int dev = 0;
@@ -60,14 +75,16 @@ cudaError_t launch_one(const PrefillParams& p, int grid, unsigned smem, cudaStre
   return cudaGetLastError();
 }
 
-template <int D, int BN, int NS, int MINB, int QT>
+template <int D, int BN, int NS, int MINB, int QT, bool SPL = false>
 cudaError_t launch_variants(const PrefillParams& p, bool win, bool bf16, int grid, unsigned smem,
                             cudaStream_t st) {
   if (win)
-    return bf16 ? launch_one<D, BN, NS, true, true, MINB, QT>(p, grid, smem, st)
-                : launch_one<D, BN, NS, true, false, MINB, QT>(p, grid, smem, st);
-  return bf16 ? launch_one<D, BN, NS, false, true, MINB, QT>(p, grid, smem, st)
-              : launch_one<D, BN, NS, false, false, MINB, QT>(p, grid, smem, st);
+    return bf16 ? launch_one<D, BN, NS, true, true, MINB, QT, SPL>(p, grid, smem, st)
+                : launch_one<D, BN, NS, true, false, MINB, QT, SPL>(p, grid, smem, st);
+  return bf16 ? launch_one<D, BN, NS, false, true, MINB, QT, SPL>(p, grid, smem, st)
+              : launch_one<D, BN, NS, false, false, MINB, QT, SPL>(p, grid, smem, st);
 }
+
+}  // namespace
 
 }  // namespace gqa

@@ -1,0 +1,132 @@
+// merge.cu -- split-KV merge: combines the fp32 partials that the split work
+// items of one unit wrote (each over a contiguous range of the unit's key
+// tiles) into out and lse, folding the sink in once.
+//
+// Split s of a row carries O_s (relative to its own reference m_s, log2
+// domain) and l_s = sum of exp2(s' - m_s) over its keys.  With
+// mf = max(max_s m_s, sink * log2 e) (the sink only when present):
+//   den = sum_s l_s exp2(m_s - mf) + [sink] exp2(sink * log2 e - mf)
+//   out = sum_s O_s exp2(m_s - mf) / den,   lse = (mf + log2 den) ln 2,
+// the log-sum-exp combine of partial softmax results (the lse_extend merge of
+// SGLang PR #34468's context-parallel path), and for one split the same value
+// the unsplit epilogue computes.  A row no split saw (all m_s = -inf) gets
+// out = 0, lse = -inf, as in the unsplit kernel.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "launch.h"
+
+namespace gqa {
+
+namespace {
+
+struct MergeParams {
+  const float* part_o;
+  const float* part_ml;
+  const int32_t* part_hdr;
+  const float* sinks;
+  void* out;
+  float* lse;
+  int num_splits, Hq, G, rows, part_rows, smooth;
+};
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ MergeParams mp) {
+  const int unit = blockIdx.x;
+  if (unit >= mp.part_hdr[0]) return;
+  const int32_t* hd = mp.part_hdr + 4 + 4 * (size_t)unit;
+  const int row0 = hd[0], g = hd[1], nvalid = hd[2];
+  const int S = mp.num_splits;
+  const float2* ml = reinterpret_cast<const float2*>(mp.part_ml);
+  const float4* po = reinterpret_cast<const float4*>(mp.part_o);
+  for (int rr = threadIdx.x; rr < mp.part_rows; rr += blockDim.x) {
+    const int r = rr % 128;
+    const int off = (rr / 128) * mp.rows + r / mp.G;  // position inside the unit
+    if (off >= nvalid) continue;
+    const int h = g * mp.G + r % mp.G;
+    const size_t orow = (size_t)(row0 + off) * mp.Hq + h;
+    uint16_t* op = reinterpret_cast<uint16_t*>(mp.out) + orow * D;
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s) M = fmaxf(M, ml[((size_t)unit * S + s) * mp.part_rows + rr].x);
+    if (M == -INFINITY) {  // no key reached this row in any split
+      uint4* dst = reinterpret_cast<uint4*>(op);
+      for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (mp.lse != nullptr) mp.lse[orow] = -INFINITY;
+      continue;
+    }
+    const bool has_x = (mp.sinks != nullptr) || (mp.smooth != 0);
+    const float ms = mp.sinks != nullptr ? mp.sinks[h] * kLog2e : 0.f;
+    const float mf = has_x ? fmaxf(M, ms) : M;
+    float den = has_x ? ex2(ms - mf) : 0.f;
+    for (int s = 0; s < S; ++s) {
+      const float2 v = ml[((size_t)unit * S + s) * mp.part_rows + rr];
+      if (v.x != -INFINITY) den += v.y * ex2(v.x - mf);
+    }
+    den = fmaxf(den, 1e-30f);
+    const float inv = 1.f / den;
+#pragma unroll 1
+    for (int c0 = 0; c0 < D / 4; c0 += 16) {  // 64 columns at a time
+      float4 acc[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s = 0; s < S; ++s) {
+        const size_t item = (size_t)unit * S + s;
+        const float m_s = ml[item * mp.part_rows + rr].x;
+        if (m_s == -INFINITY) continue;  // an empty split carries no O
+        const float w = ex2(m_s - mf) * inv;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float4 o = po[(item * (D / 4) + c0 + i) * mp.part_rows + rr];
+          acc[i].x += w * o.x;
+          acc[i].y += w * o.y;
+          acc[i].z += w * o.z;
+          acc[i].w += w * o.w;
+        }
+      }
+      uint4* dst = reinterpret_cast<uint4*>(op + c0 * 4);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        dst[i] = make_uint4(pack2<BF16>(acc[2 * i].x, acc[2 * i].y),
+                            pack2<BF16>(acc[2 * i].z, acc[2 * i].w),
+                            pack2<BF16>(acc[2 * i + 1].x, acc[2 * i + 1].y),
+                            pack2<BF16>(acc[2 * i + 1].z, acc[2 * i + 1].w));
+    }
+    if (mp.lse != nullptr) mp.lse[orow] = (mf + log2f(den)) * kLn2;
+  }
+}
+
+template <int D>
+cudaError_t launch_merge_d(const MergeParams& mp, bool bf16, int grid, cudaStream_t st) {
+  if (bf16)
+    merge_kernel<D, true><<<grid, 128, 0, st>>>(mp);
+  else
+    merge_kernel<D, false><<<grid, 128, 0, st>>>(mp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const PrefillParams& p, int d, bool bf16, int part_rows, int grid,
+                         cudaStream_t st) {
+  MergeParams mp;
+  mp.part_o = p.part_o;
+  mp.part_ml = p.part_ml;
+  mp.part_hdr = p.part_hdr;
+  mp.sinks = p.sinks;
+  mp.out = p.out;
+  mp.lse = p.lse;
+  mp.num_splits = p.num_splits;
+  mp.Hq = p.Hq;
+  mp.G = p.G;
+  mp.rows = p.rows;
+  mp.part_rows = part_rows;
+  mp.smooth = p.smooth;
+  if (grid < 1) return cudaSuccess;
+  if (d == 64) return launch_merge_d<64>(mp, bf16, grid, st);
+  if (d == 128) return launch_merge_d<128>(mp, bf16, grid, st);
+  if (d == 256) return launch_merge_d<256>(mp, bf16, grid, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace gqa

@@ -64,6 +64,13 @@ struct PrefillParams {
   int smooth;
   float scale_log2;      // scale * log2(e)
   unsigned long long timeout_ns;
+  // Split-KV (num_splits > 1): work item i is split i % num_splits of unit
+  // i / num_splits, a contiguous range of the unit's key tiles.  Items write
+  // fp32 partials instead of out / lse; merge_kernel combines them.
+  int num_splits;
+  float* part_o;      // unnormalised O: [item][d/4][QT*128 rows][4]
+  float* part_ml;     // (m in the log2 domain, l) per row: [item][QT*128][2]
+  int32_t* part_hdr;  // [0] units; [4 + 4 u ..] (first q row, KV head, valid positions, 0)
 };
 
 __host__ __device__ constexpr int pow2_cols(int n) {
@@ -113,6 +120,7 @@ struct Bar {
 
 struct Unit {
   int b, g, q0, q_last, P, E, kv_base, q_row0, kv_lo, n_tiles;
+  int id;  // unit number (differs from the work item under split-KV)
 };
 
 // Per-sequence metadata copied into shared memory once per CTA, so that
@@ -150,6 +158,28 @@ __device__ __forceinline__ Unit decode_unit(const PrefillParams& p, const SeqTab
   const KvRange r = kv_range(U.P, U.q0, U.q_last, p.window, BN);
   U.kv_lo = r.kv_lo;
   U.n_tiles = r.n_tiles;
+  return U;
+}
+
+// Work item -> unit and key-tile range.  Without split-KV an item is a unit;
+// with it, split s of S takes the unit's tiles [s n / S, (s + 1) n / S), which
+// may be empty when the unit has fewer than S tiles.
+template <bool SPL>
+__device__ __forceinline__ Unit decode_item(const PrefillParams& p, const SeqTab& T, int item,
+                                            int BN, int urows) {
+  if (!SPL) {
+    Unit U = decode_unit(p, T, item, BN, urows);
+    U.id = item;
+    return U;
+  }
+  const int S = p.num_splits;
+  const int unit = item / S, s = item - unit * S;
+  Unit U = decode_unit(p, T, unit, BN, urows);
+  U.id = unit;
+  const int n = U.n_tiles;  // n * S < 2^31: at most 16 splits of a KV range below 2^27 tiles
+  const int t0 = s * n / S, t1 = (s + 1) * n / S;
+  U.kv_lo += t0 * BN;
+  U.n_tiles = t1 - t0;
   return U;
 }
 
@@ -201,7 +231,9 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity,
 }
 
 
-template <int D, int BN, int NS, bool WIN, bool BF16, int MINB, int QT>
+// SPL: split-KV work items writing partials (a separate instantiation, so the
+// unsplit kernel carries none of its code).
+template <int D, int BN, int NS, bool WIN, bool BF16, int MINB, int QT, bool SPL>
 __global__ void __launch_bounds__(threads_for(QT), MINB)
     prefill_kernel(const __grid_constant__ PrefillParams p) {
   static_assert(D == 64 || D == 128 || D == 256, "head dim");
@@ -322,10 +354,15 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
   }
   __syncthreads();
   if (misc[2] != 0u) {
-    if (tid == 0) atomicOr(p.status, 2u);  // GQA_DEV_BAD_METADATA
+    if (tid == 0) {
+      atomicOr(p.status, 2u);  // GQA_DEV_BAD_METADATA
+      if (SPL && blockIdx.x == 0) p.part_hdr[0] = 0;  // nothing to merge
+    }
     return;
   }
-  const int n_units = tile_start[nseq] * p.Hkv;
+  // Work items: units, times the split count under split-KV.
+  const int n_units = tile_start[nseq] * p.Hkv * (SPL ? p.num_splits : 1);
+  if (SPL && blockIdx.x == 0 && tid == 0) p.part_hdr[0] = tile_start[nseq] * p.Hkv;
   if (blockIdx.x >= n_units) return;  // nothing for this CTA (before any TMEM use)
 
   if (warp == kMmaWarp) {
@@ -351,7 +388,8 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
       for (int kk = 0;; ++kk) {
         const int uk = unit_of(kk);
         if (uk >= n_units) break;
-        const Unit U = decode_unit(p, T, uk, BN, urows);
+        const Unit U = decode_item<SPL>(p, T, uk, BN, urows);
+        if (SPL && U.n_tiles == 0) continue;  // empty split: no loads, no Q buffer
         const uint32_t qb = nq % NQ;
         if (!wait_bounded(sBar + 8u * (B::kQEmpty + qb), ((nq / NQ) & 1u) ^ 1u, abort_flag,
                           p.status, tmo))
@@ -395,7 +433,7 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
       for (int kv = 0; ok; ++kv) {
         const int uv = unit_of(kv);
         if (uv >= n_units) break;
-        const Unit U = decode_unit(p, T, uv, BN, urows);
+        const Unit U = decode_item<SPL>(p, T, uv, BN, urows);
         for (int j = 0; j < U.n_tiles; ++j, ++itv) {
           const uint32_t s = itv % NS, ph = (itv / NS) & 1u;
           if (!(ok = wait_bounded(sBar + 8u * (B::kVEmpty + s), ph ^ 1u, abort_flag, p.status, tmo)))
@@ -458,12 +496,13 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
     bool ok = true;
     int u = unit_of(0);
     Unit Un;
-    if (u < n_units) Un = decode_unit(p, T, u, BN, urows);
+    if (u < n_units) Un = decode_item<SPL>(p, T, u, BN, urows);
     for (int k = 0; ok && u < n_units; ++k) {
       const Unit U = Un;  // decoded one unit ahead: its loads overlap this unit
       const int u_next = unit_of(k + 1);
-      if (u_next < n_units) Un = decode_unit(p, T, u_next, BN, urows);
+      if (u_next < n_units) Un = decode_item<SPL>(p, T, u_next, BN, urows);
       u = u_next;
+      if (SPL && U.n_tiles == 0) continue;  // empty split: nothing to issue
       const uint32_t qb = uc % NQ;
       if (!(ok = wait_all(sBar + 8u * (B::kQFull + qb), (uc / NQ) & 1u))) break;
       for (int j = 0; j < U.n_tiles; ++j) {
@@ -510,11 +549,15 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
     bool release_pending = false;  // Q buffer to hand back after the next P store
     uint32_t release_qb = 0;
     uint32_t n_full = 0;  // units whose output went through the TMA store
+    uint32_t kq = 0;      // non-empty items done (they take Q buffers in turn)
+    constexpr bool split = SPL;
+    const int part_rows = QT * 128;  // partial rows per work item
+    const int rr = sub * 128 + r;     // this thread's partial row
     int u = unit_of(0);
     Unit Un;
     float sink_next = 0.f;
     if (u < n_units) {
-      Un = decode_unit(p, T, u, BN, urows);
+      Un = decode_item<SPL>(p, T, u, BN, urows);
       if (p.sinks != nullptr) sink_next = __ldg(p.sinks + Un.g * p.G + r % p.G);
     }
     for (int k = 0; ok && u < n_units; ++k) {
@@ -523,12 +566,25 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
       const Unit U = Un;
       const int cur_u = u;
       const float sink = sink_next;
-      const uint32_t qb = (uint32_t)k % NQ;  // this unit's Q buffer
       u = unit_of(k + 1);
       if (u < n_units) {
-        Un = decode_unit(p, T, u, BN, urows);
+        Un = decode_item<SPL>(p, T, u, BN, urows);
         if (p.sinks != nullptr) sink_next = __ldg(p.sinks + Un.g * p.G + r % p.G);
       }
+      if (split && leader && sub == 0) {  // where the merge writes this unit's rows
+        int32_t* hd = p.part_hdr + 4 + 4 * (size_t)U.id;
+        hd[0] = U.q_row0;
+        hd[1] = U.g;
+        hd[2] = U.q_last - U.q0 + 1;
+        hd[3] = 0;
+      }
+      if (split && U.n_tiles == 0) {  // empty split: a record the merge gives weight 0
+        reinterpret_cast<float2*>(p.part_ml)[(size_t)cur_u * part_rows + rr] =
+            make_float2(-INFINITY, 0.f);
+        continue;
+      }
+      const uint32_t qb = (SPL ? kq : (uint32_t)k) % NQ;  // this unit's Q buffer
+      ++kq;
       // This warpgroup's query tile: positions [q0s, qls] (empty when qls < q0s,
       // a unit's second tile past the end of its sequence).
       const int q0s = U.q0 + sub * p.rows;
@@ -707,6 +763,28 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
                                                  ((it - 1u) / NP) & 1u, abort_flag, p.status, tmo));
       if (!ok) break;
       tc_fence_after();
+      if constexpr (split) {
+        // Partial of one key range: O relative to m, unnormalised, with (m, l);
+        // float4 (c4, row) order so that a warp's stores are contiguous.
+        float4* po = reinterpret_cast<float4*>(p.part_o) + (size_t)cur_u * (D / 4) * part_rows;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(t_lane + kColO + c * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            po[(size_t)(c * 8 + i) * part_rows + rr] =
+                make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                            __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+        }
+        reinterpret_cast<float2*>(p.part_ml)[(size_t)cur_u * part_rows + rr] = make_float2(m, l);
+        // Nothing staged in the Q buffer: hand it back once the O reads are done.
+        tc_fence_before();
+        __syncwarp();
+        if (leader) mbar_arrive(sBar + 8u * (B::kQEmpty + qb));
+        continue;
+      }
       const bool has_x = (p.sinks != nullptr) || (p.smooth != 0);
       const float ms = sink * kLog2e;  // 0 in smooth mode
       float inv = 0.f, lse2 = -INFINITY;

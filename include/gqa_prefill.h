@@ -63,7 +63,15 @@
 #ifndef GQA_PREFILL_H
 #define GQA_PREFILL_H
 
+#include <stddef.h>
 #include <stdint.h>
+
+/* Symbols of the C ABI; the library is built with hidden visibility otherwise. */
+#if defined(__GNUC__)
+#define GQA_API __attribute__((visibility("default")))
+#else
+#define GQA_API
+#endif
 
 #ifdef __cplusplus
 extern "C" {
@@ -103,12 +111,58 @@ enum {
  *   smooth_softmax nonzero: +1 in the denominator (sinks must be NULL)
  * Returns GQA_OK or a negative GQA_ERR_* code.
  */
-int gqa_flash_prefill(const void* q, const void* k, const void* v,
+GQA_API int gqa_flash_prefill(const void* q, const void* k, const void* v,
                       const int32_t* cu_seqlens_q, const int32_t* prefix_lens,
                       const int32_t* kv_indptr, int num_seqs, int total_q,
                       int total_kv, int max_seqlen_q, int Hq, int Hkv, int d,
                       int dtype, float scale, int window, const float* sinks,
                       int smooth_softmax, void* out, float* lse, void* stream);
+
+/*
+ * gqa_flash_prefill_splitkv -- the same operation as gqa_flash_prefill, with
+ * each work unit's key tiles divided into num_splits contiguous ranges
+ * processed by separate CTAs, for calls whose units would not fill the GPU
+ * (short query chunks over long cached prefixes).  Each range produces an
+ * fp32 partial (O relative to its own running maximum, the maximum, the
+ * denominator); a second kernel combines the partials of a unit with the
+ * log-sum-exp merge and folds the sink in once, the partial-result combine
+ * that SGLang PR #34468 ("gfx950 SWA prefix trim") uses for its
+ * context-parallel path.  The result equals the unsplit call up to rounding.
+ *
+ *   num_splits       0: the library's choice (splits only when the units fill
+ *                    less than half the resident CTAs), else 1..16; 1 is the
+ *                    unsplit kernel and needs no workspace.
+ *   workspace        device memory owned by the caller, 256-byte aligned, at
+ *                    least the size gqa_prefill_splitkv_workspace() reports
+ *                    for the same shapes and num_splits; only scratch (its
+ *                    contents before and after the call are meaningless), and
+ *                    must not be shared by calls that may run concurrently.
+ *   workspace_bytes  its size.
+ *
+ * Other arguments, layouts and return codes as gqa_flash_prefill; a missing
+ * or too small workspace returns GQA_ERR_INVALID before any launch.  Two
+ * kernels are enqueued on `stream`.
+ */
+GQA_API int gqa_flash_prefill_splitkv(const void* q, const void* k, const void* v,
+                              const int32_t* cu_seqlens_q,
+                              const int32_t* prefix_lens, const int32_t* kv_indptr,
+                              int num_seqs, int total_q, int total_kv,
+                              int max_seqlen_q, int Hq, int Hkv, int d, int dtype,
+                              float scale, int window, const float* sinks,
+                              int smooth_softmax, void* out, float* lse,
+                              int num_splits, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
+ * Host only: the split count gqa_flash_prefill_splitkv will use for these
+ * shapes and num_splits (0 = the library's choice) in *splits_used, and the
+ * workspace it needs in *bytes (0 when the call does not split).  Returns
+ * GQA_OK, GQA_ERR_INVALID or GQA_ERR_UNSUPPORTED as gqa_prefill_plan.
+ */
+GQA_API int gqa_prefill_splitkv_workspace(int num_seqs, int total_q, int max_seqlen_q,
+                                  int Hq, int Hkv, int d, int dtype, int window,
+                                  int num_splits, int* splits_used,
+                                  size_t* bytes);
 
 /*
  * Launch plan of a call with these shapes (host only, no device access).
@@ -128,7 +182,7 @@ typedef struct {
     int q_tiles;        /* 128-row query tiles per unit: 1, or 2 (one CTA per SM) */
 } gqa_prefill_plan_t;
 
-int gqa_prefill_plan(int num_seqs, int total_q, int max_seqlen_q, int Hq,
+GQA_API int gqa_prefill_plan(int num_seqs, int total_q, int max_seqlen_q, int Hq,
                      int Hkv, int d, int dtype, int window,
                      gqa_prefill_plan_t* plan);
 
@@ -142,7 +196,7 @@ int gqa_prefill_plan(int num_seqs, int total_q, int max_seqlen_q, int Hq,
  * sequence's first key), n_masked how many of them needed the per-element
  * mask, cta the CTA that ran it and order its position in that CTA's list.
  */
-int gqa_flash_prefill_debug(const void* q, const void* k, const void* v,
+GQA_API int gqa_flash_prefill_debug(const void* q, const void* k, const void* v,
                             const int32_t* cu_seqlens_q,
                             const int32_t* prefix_lens, const int32_t* kv_indptr,
                             int num_seqs, int total_q, int total_kv,
@@ -158,7 +212,7 @@ int gqa_flash_prefill_debug(const void* q, const void* k, const void* v,
  * the forced size returns GQA_ERR_UNSUPPORTED).  Returns GQA_OK or
  * GQA_ERR_INVALID.  Meant for tests and tuning.
  */
-int gqa_prefill_force_block_n(int block_n);
+GQA_API int gqa_prefill_force_block_n(int block_n);
 
 /*
  * Force the number of 128-row query tiles per work unit for later calls in
@@ -169,7 +223,7 @@ int gqa_prefill_force_block_n(int block_n);
  * kernel returns GQA_ERR_UNSUPPORTED.  Returns GQA_OK or GQA_ERR_INVALID.
  * Meant for tests and tuning.
  */
-int gqa_prefill_force_q_tiles(int q_tiles);
+GQA_API int gqa_prefill_force_q_tiles(int q_tiles);
 
 /*
  * Launch-configuration tuning.  The configuration cache is keyed on (d, a
@@ -183,17 +237,17 @@ int gqa_prefill_force_q_tiles(int q_tiles);
  * while the stream is being captured.  GQA_PREFILL_TUNE_DEBUG=1 prints the
  * timings.  enable: 0 or 1.  Returns GQA_OK or GQA_ERR_INVALID.
  */
-int gqa_prefill_set_tuning(int enable);
+GQA_API int gqa_prefill_set_tuning(int enable);
 
 /* Forget every cached configuration (tuned or default).  Returns GQA_OK. */
-int gqa_prefill_clear_config_cache(void);
+GQA_API int gqa_prefill_clear_config_cache(void);
 
 /*
  * The cached configuration for a call with these shapes: *block_n = 0 (and
  * *q_tiles = 0) if the key has no entry yet; *tuned = 1 if the entry came
  * from a timed sweep.  q_tiles may be NULL.
  */
-int gqa_prefill_config_block_n(int total_q, int max_seqlen_q, int Hq, int Hkv,
+GQA_API int gqa_prefill_config_block_n(int total_q, int max_seqlen_q, int Hq, int Hkv,
                                int d, int dtype, int window, int* block_n,
                                int* q_tiles, int* tuned);
 
@@ -205,20 +259,20 @@ int gqa_prefill_config_block_n(int total_q, int max_seqlen_q, int Hq, int Hkv,
  * reads and clears the status word into *status (expected GQA_DEV_TIMEOUT).
  * The CUDA context stays usable afterwards.
  */
-int gqa_prefill_selftest_timeout(int timeout_ms, void* stream, int* status);
+GQA_API int gqa_prefill_selftest_timeout(int timeout_ms, void* stream, int* status);
 
 /*
  * Read and clear the device status word of the current device (bits
  * GQA_DEV_*).  Synchronises the device first.  Returns GQA_OK or
  * GQA_ERR_CUDA; *status receives the bits.
  */
-int gqa_prefill_get_device_status(int* status);
+GQA_API int gqa_prefill_get_device_status(int* status);
 
 /* Static text for a GQA_* return code. */
-const char* gqa_prefill_status_string(int code);
+GQA_API const char* gqa_prefill_status_string(int code);
 
 /* Library version, e.g. "0.1.0". */
-const char* gqa_prefill_version(void);
+GQA_API const char* gqa_prefill_version(void);
 
 #ifdef __cplusplus
 }
