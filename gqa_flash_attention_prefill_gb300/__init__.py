@@ -15,6 +15,8 @@ from typing import Optional
 __all__ = ["load", "gqa_flash_prefill", "gqa_flash_prefill_debug", "prefill",
            "plan", "force_block_n", "force_q_tiles", "get_device_status", "set_tuning",
            "gqa_flash_prefill_splitkv", "splitkv_workspace", "prefill_splitkv",
+           "gqa_flash_prefill_splitkv_noalloc", "prefill_splitkv_noalloc",
+           "NOALLOC_SCRATCH_BYTES",
            "clear_config_cache", "config_block_n", "selftest_timeout", "GQAError",
            "GQA_F16", "GQA_BF16", "GQA_DEV_TIMEOUT", "GQA_DEV_BAD_METADATA",
            "EXPORTED_SYMBOLS"]
@@ -30,7 +32,9 @@ EXPORTED_SYMBOLS = [
     "gqa_prefill_clear_config_cache", "gqa_prefill_config_block_n",
     "gqa_prefill_selftest_timeout", "gqa_prefill_force_q_tiles",
     "gqa_flash_prefill_splitkv", "gqa_prefill_splitkv_workspace",
+    "gqa_flash_prefill_splitkv_noalloc",
 ]
+NOALLOC_SCRATCH_BYTES = 32 << 20  # the library's file-scope split-KV scratch (gqa_prefill.h)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgqa_prefill.so")
@@ -72,6 +76,8 @@ def load(path: Optional[str] = None):
     lib.gqa_flash_prefill_debug.restype = ctypes.c_int
     lib.gqa_flash_prefill_splitkv.argtypes = core[:-1] + [ctypes.c_int, vp, ctypes.c_size_t, vp]
     lib.gqa_flash_prefill_splitkv.restype = ctypes.c_int
+    lib.gqa_flash_prefill_splitkv_noalloc.argtypes = core[:-1] + [ctypes.c_int, vp]
+    lib.gqa_flash_prefill_splitkv_noalloc.restype = ctypes.c_int
     lib.gqa_prefill_splitkv_workspace.argtypes = [ctypes.c_int] * 9 + [
         ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_size_t)]
     lib.gqa_prefill_splitkv_workspace.restype = ctypes.c_int
@@ -205,6 +211,30 @@ def splitkv_workspace(num_seqs, total_q, max_seqlen_q, hq, hkv, d, dtype, window
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_prefill_splitkv_workspace")
     return used.value, nbytes.value
+
+
+def gqa_flash_prefill_splitkv_noalloc(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, scale,
+                                      num_splits=0, window=0, sinks=None, smooth_softmax=False,
+                                      out=None, lse=None, stream=None, max_seqlen_q=0):
+    """Split-KV with the library's file-scope scratch (see gqa_prefill.h): no
+    workspace, nothing allocated; overlapping calls race on the scratch."""
+    a = _args(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, scale, window, sinks,
+              smooth_softmax, out, lse, stream, max_seqlen_q)
+    rc = load().gqa_flash_prefill_splitkv_noalloc(*a[:-1], int(num_splits), a[-1])
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_flash_prefill_splitkv_noalloc")
+    return out
+
+
+def prefill_splitkv_noalloc(batch, num_splits=0, out=None, lse=None, stream=None):
+    """gqa_flash_prefill_splitkv_noalloc on one ``workloads.Batch`` already on
+    the GPU, into caller buffers (out is required: the call allocates nothing)."""
+    gqa_flash_prefill_splitkv_noalloc(batch.q, batch.k, batch.v, batch.cu_seqlens_q,
+                                      batch.prefix_lens, batch.kv_indptr, batch.scale,
+                                      num_splits=num_splits, window=batch.window,
+                                      sinks=batch.sinks, smooth_softmax=batch.smooth, out=out,
+                                      lse=lse, stream=stream, max_seqlen_q=batch.max_seqlen_q)
+    return out, lse
 
 
 def prefill_splitkv(batch, num_splits=0, workspace=None, out=None, lse=None, with_lse=True,

@@ -154,6 +154,34 @@ GQA_API int gqa_flash_prefill_splitkv(const void* q, const void* k, const void* 
                               size_t workspace_bytes, void* stream);
 
 /*
+ * gqa_flash_prefill_splitkv_noalloc -- gqa_flash_prefill_splitkv without a
+ * caller workspace: the partials live in a 32 MiB (33,554,432-byte) array of
+ * device memory defined at file scope in the library, so the call allocates
+ * nothing.  The paper has no counterpart; the entry point exists for callers
+ * that may not allocate device memory.
+ *
+ *   num_splits  as gqa_flash_prefill_splitkv (0 = the library's choice).
+ *
+ * Shapes whose split-KV workspace (gqa_prefill_splitkv_workspace for the same
+ * arguments) exceeds the array return GQA_ERR_UNSUPPORTED before any launch.
+ * Nothing in the array has to start at zero: every value the merge reads is
+ * written earlier in the same call.  The array is one per device and process:
+ * calls that overlap in time on a device (other streams, other host threads)
+ * race on it, so the caller must order them.  Other arguments, layouts and
+ * return codes as gqa_flash_prefill; GQA_ERR_CUDA if the array's address
+ * cannot be obtained.
+ */
+GQA_API int gqa_flash_prefill_splitkv_noalloc(const void* q, const void* k, const void* v,
+                                              const int32_t* cu_seqlens_q,
+                                              const int32_t* prefix_lens,
+                                              const int32_t* kv_indptr, int num_seqs,
+                                              int total_q, int total_kv, int max_seqlen_q,
+                                              int Hq, int Hkv, int d, int dtype, float scale,
+                                              int window, const float* sinks,
+                                              int smooth_softmax, void* out, float* lse,
+                                              int num_splits, void* stream);
+
+/*
  * Host only: the split count gqa_flash_prefill_splitkv will use for these
  * shapes and num_splits (0 = the library's choice) in *splits_used, and the
  * workspace it needs in *bytes (0 when the call does not split).  Returns
