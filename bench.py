@@ -352,6 +352,14 @@ def run_workload(args, rank, world):
         desc = ("ragged varlen: 16 sequences, prefixes U[0,16384], extends U[1,8192], 64/8, d 64, "
                 "bf16, window 128, sinks")
         tokens = b.total_q
+    elif args.workload == "decode":
+        b = W.decode(num_seqs=128, min_prefix=1024, max_prefix=16384, window=128,
+                     sink_mode="head", seed=6,
+                     window_bounded_layout=(args.layout == "window-bounded"))
+        calls = [b.to(dev)]
+        desc = (f"windowed decode: 128 sequences x 1 new token over prefixes U[1024,16384], "
+                f"64/8, d 64, bf16, window 128, sinks, {args.layout} KV layout")
+        tokens = 128
     elif args.workload == "short_chunk":
         calls = [W.make_batch([16384, 16384], [64, 64], 64, 8, 64, "bf16", window=w,
                               sink_mode="head", seed=5 + i, name=f"short-chunk-w{w}").to(dev)
@@ -421,7 +429,7 @@ def run_workload(args, rank, world):
             "pct_of_bf16_peak": round(100.0 * value / (world * peaks["bf16_tflops"]), 2),
             "gpu_launches": len(calls) * args.steps + sum(1 for s_ in splits_used if s_ > 1) * args.steps,
             "clocks": clk.summary()}
-    if args.workload == "chunked_prefix":
+    if args.workload in ("chunked_prefix", "decode"):
         # HBM-bound: Q read and O (+ lse) written once; of K and V only the rows some
         # window reaches (the window-bounded layout's rows) must be read, in either layout.
         nbytes = 0
@@ -542,11 +550,12 @@ def main():
                     help="CPU work of the oracle baseline sample (rank 0, N=1)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="layer_pair",
-                    choices=["layer_pair", "chunked_prefix", "oss20b_16k", "ragged", "short_chunk"],
+                    choices=["layer_pair", "chunked_prefix", "oss20b_16k", "ragged", "short_chunk",
+                             "decode"],
                     help="layer_pair is the headline configuration; the others are "
                          "supplementary measurements")
     ap.add_argument("--layout", default="window-bounded", choices=["window-bounded", "full-prefix"],
-                    help="KV layout of the chunked_prefix workload")
+                    help="KV layout of the chunked_prefix and decode workloads")
     ap.add_argument("--splits", type=int, default=-1,
                     help="supplementary workloads: -1 the plain entry point; 0 split-KV with "
                          "the library's split count; k >= 1 split-KV with k splits")

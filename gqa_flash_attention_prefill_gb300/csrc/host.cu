@@ -479,9 +479,13 @@ int tune_key(const void* q, const void* k, const void* v, const int32_t* cu_seql
 }
 
 // Split count for a plan: `req` 0 = the library's choice, else 1..kMaxSplits.
-int splits_for(const Plan& pl, int total_q, int Hkv, int req) {
+// The unit count is estimated from below without reading device metadata:
+// the tokens packed into units, and at least one unit per sequence and KV head
+// (a decode step of many one-token sequences has many units).
+int splits_for(const Plan& pl, int num_seqs, int total_q, int Hkv, int req) {
   if (req != 0) return req;
-  const long long units = (long long)Hkv * ((total_q + pl.unit_rows - 1) / pl.unit_rows);
+  const long long packed = (total_q + pl.unit_rows - 1) / pl.unit_rows;
+  const long long units = (long long)Hkv * (packed > num_seqs ? packed : num_seqs);
   return choose_splits(units > (1ll << 30) ? (1 << 30) : (int)units, pl.slots);
 }
 
@@ -492,12 +496,12 @@ int plan_split(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, int
                int window, int req, Plan* pl, int* S) {
   int rc = make_plan(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, pl);
   if (rc != GQA_OK) return rc;
-  *S = splits_for(*pl, total_q, Hkv, req);
+  *S = splits_for(*pl, num_seqs, total_q, Hkv, req);
   if (*S > 1 && !split_shape(d, pl->shape.block_n, pl->shape.q_tiles)) {
     const int bn = split_shape(d, pl->shape.block_n, 1) ? pl->shape.block_n : (d == 64 ? 128 : 64);
     rc = make_plan_bn(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, bn, 1, pl);
     if (rc != GQA_OK) return rc;
-    *S = splits_for(*pl, total_q, Hkv, req);
+    *S = splits_for(*pl, num_seqs, total_q, Hkv, req);
   }
   return GQA_OK;
 }

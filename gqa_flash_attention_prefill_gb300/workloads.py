@@ -225,3 +225,17 @@ def ragged(num_seqs: int = 16, max_prefix: int = 16384, max_extend: int = 8192,
     return make_batch(pre, ext, hq, hkv, d, dtype, window=window,
                       sink_mode=sink_mode, seed=seed,
                       name=f"ragged-{num_seqs}-h{hq}/{hkv}-d{d}-{dtype}-w{window}-{sink_mode}")
+
+
+def decode(num_seqs: int = 128, min_prefix: int = 1024, max_prefix: int = 16384,
+           hq: int = 64, hkv: int = 8, d: int = 64, dtype: str = "bf16", window: int = 128,
+           sink_mode: str = "head", seed: int = 6, window_bounded_layout: bool = False) -> Batch:
+    """Decode step: one new token per sequence over a cached prefix drawn
+    uniformly in [min_prefix, max_prefix] (once per seed).  With
+    window_bounded_layout the batch carries only the last min(prefix, window)
+    prefix rows of each sequence."""
+    gen = torch.Generator().manual_seed(int(seed) * 104729 + 3)
+    pre = torch.randint(min_prefix, max_prefix + 1, (num_seqs,), generator=gen).tolist()
+    b = make_batch(pre, [1] * num_seqs, hq, hkv, d, dtype, window=window, sink_mode=sink_mode,
+                   seed=seed, name=f"decode-{num_seqs}-h{hq}/{hkv}-d{d}-{dtype}-w{window}")
+    return window_bounded(b, window) if (window_bounded_layout and window > 0) else b

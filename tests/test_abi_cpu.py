@@ -136,3 +136,19 @@ def test_binding_refuses_to_run_without_library(tmp_path):
     import gqa_flash_attention_prefill_gb300 as pkg
     with pytest.raises(RuntimeError, match="missing"):
         pkg.load(str(tmp_path / "nope.so"))
+
+
+def test_split_count_choice_is_host_only(lib):
+    """The library's split-KV choice, from shapes alone (no device access):
+    no split when the units fill the GPU (a 4096-token prefill, a decode step
+    of 128 sequences), splits when they cannot (two 64-token chunks, a
+    four-sequence decode step); explicit counts are honoured up to 16."""
+    import gqa_flash_attention_prefill_gb300 as pkg
+    assert pkg.splitkv_workspace(1, 4096, 4096, 64, 8, 64, "bf16", 0, 0) == (1, 0)
+    assert pkg.splitkv_workspace(128, 128, 1, 64, 8, 64, "bf16", 128, 0) == (1, 0)
+    used, nbytes = pkg.splitkv_workspace(2, 128, 64, 64, 8, 64, "bf16", 0, 0)
+    assert used > 1 and nbytes > 0
+    used, nbytes = pkg.splitkv_workspace(4, 4, 1, 64, 8, 64, "bf16", 0, 0)
+    assert used > 1 and nbytes > 0
+    used, nbytes = pkg.splitkv_workspace(1, 64, 64, 64, 8, 64, "bf16", 0, 16)
+    assert used == 16 and nbytes > 0

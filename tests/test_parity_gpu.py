@@ -315,3 +315,32 @@ def test_counting_probe_exact_key_sets(pkg, dtype, window, q_tiles):
             row = cu[s] + i
             assert bool((n[row] == want_n).all()), (s, i, n[row], want_n)
             assert bool((counts[row] == want).all()), (s, i)
+
+
+# ------------------------------------------------------------- decode (one token per sequence)
+
+@pytest.mark.parametrize("window", [1, 64, 128, 129, 0])
+@pytest.mark.parametrize("sink_mode", ["head", "smooth", "none"])
+def test_decode_full_output(pkg, window, sink_mode):
+    """One new token per sequence over cached prefixes (full-prefix layout)."""
+    b = W.decode(num_seqs=24, min_prefix=0, max_prefix=3000, window=window,
+                 sink_mode=sink_mode, seed=40 + window)
+    _check_full(pkg, b)
+
+
+def test_decode_layouts_agree(pkg):
+    full = W.decode(num_seqs=32, min_prefix=100, max_prefix=5000, window=128, seed=41)
+    bounded = W.window_bounded(full, 128)
+    a_out, a_lse = run_gpu(pkg, full)
+    b_out, b_lse = run_gpu(pkg, bounded)
+    ref, ref_lse = run_oracle(full)
+    compare(a_out, a_lse, ref, ref_lse, label="decode full-prefix layout")
+    compare(b_out, b_lse, ref, ref_lse, label="decode window-bounded layout")
+
+
+def test_decode_tiles_bounded_by_window(pkg):
+    """Each decode unit walks at most ceil(w / BN) + 1 key tiles whatever its
+    prefix (bit-exact bookkeeping against the oracle census)."""
+    b = W.decode(num_seqs=16, min_prefix=0, max_prefix=20000, window=128, seed=42)
+    p, used = _bookkeeping(pkg, b)
+    assert int(used[:, 4].max()) <= -(-128 // p["block_n"]) + 1

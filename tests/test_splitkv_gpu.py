@@ -141,3 +141,14 @@ def test_split_bad_metadata_writes_nothing(pkg):
     torch.cuda.synchronize()
     assert pkg.get_device_status() == pkg.GQA_DEV_BAD_METADATA
     assert bool((out == 7.0).all())
+
+
+def test_split_decode_few_sequences_long_prefix(pkg):
+    """Decode of a few sequences over long full-attention prefixes: a handful
+    of units, so the library splits."""
+    b = W.decode(num_seqs=4, min_prefix=4000, max_prefix=6000, window=0, sink_mode="head",
+                 seed=43)
+    used, _ = pkg.splitkv_workspace(b.num_seqs, b.total_q, b.max_seqlen_q, b.hq, b.hkv, b.d,
+                                    "bf16", 0, 0)
+    assert used > 1
+    check(pkg, b, 0, label="decode, auto split")
