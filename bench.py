@@ -387,9 +387,15 @@ def run_workload(args, rank, world):
             splits_used.append(used)
             workspaces.append(torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev))
 
+    # --paged P: the same K/V laid out as a shuffled pool of P-token pages.
+    paged_calls = ([W.paged(b.to("cpu"), args.paged, seed=i).to(dev) for i, b in enumerate(calls)]
+                   if args.paged > 0 else [])
+
     def step():
         for i, (b, o, l) in enumerate(zip(calls, outs, lses)):
-            if args.splits >= 0:
+            if args.paged > 0:
+                pkg.prefill_paged(paged_calls[i], out=o, lse=l, stream=stream)
+            elif args.splits >= 0:
                 pkg.prefill_splitkv(b, num_splits=args.splits, workspace=workspaces[i], out=o,
                                     lse=l, stream=stream)
             else:
@@ -423,8 +429,10 @@ def run_workload(args, rank, world):
             "data": "synthetic (seeded N(0,1) Q/K/V and sinks; no model weights)",
             "config": {"workload": desc, "l2": "flushed between steps (256 MiB write)",
                        "calls_per_step": len(calls),
-                       "entry": ("gqa_flash_prefill_splitkv, splits " + str(splits_used))
-                       if args.splits >= 0 else "gqa_flash_prefill"},
+                       "entry": (f"gqa_flash_prefill_paged, page_size {args.paged}"
+                                 if args.paged > 0 else
+                                 ("gqa_flash_prefill_splitkv, splits " + str(splits_used))
+                                 if args.splits >= 0 else "gqa_flash_prefill")},
             "tokens_per_s": round(world * tokens / (ms_step * 1e-3), 1),
             "pct_of_bf16_peak": round(100.0 * value / (world * peaks["bf16_tflops"]), 2),
             "gpu_launches": len(calls) * args.steps + sum(1 for s_ in splits_used if s_ > 1) * args.steps,
@@ -556,6 +564,9 @@ def main():
                          "supplementary measurements")
     ap.add_argument("--layout", default="window-bounded", choices=["window-bounded", "full-prefix"],
                     help="KV layout of the chunked_prefix and decode workloads")
+    ap.add_argument("--paged", type=int, default=0,
+                    help="supplementary workloads: K/V as a page pool with this page size "
+                         "(0: contiguous)")
     ap.add_argument("--splits", type=int, default=-1,
                     help="supplementary workloads: -1 the plain entry point; 0 split-KV with "
                          "the library's split count; k >= 1 split-KV with k splits")

@@ -16,7 +16,7 @@ __all__ = ["load", "gqa_flash_prefill", "gqa_flash_prefill_debug", "prefill",
            "plan", "force_block_n", "force_q_tiles", "get_device_status", "set_tuning",
            "gqa_flash_prefill_splitkv", "splitkv_workspace", "prefill_splitkv",
            "gqa_flash_prefill_splitkv_noalloc", "prefill_splitkv_noalloc",
-           "NOALLOC_SCRATCH_BYTES",
+           "NOALLOC_SCRATCH_BYTES", "gqa_flash_prefill_paged", "prefill_paged",
            "clear_config_cache", "config_block_n", "selftest_timeout", "GQAError",
            "GQA_F16", "GQA_BF16", "GQA_DEV_TIMEOUT", "GQA_DEV_BAD_METADATA",
            "EXPORTED_SYMBOLS"]
@@ -32,7 +32,7 @@ EXPORTED_SYMBOLS = [
     "gqa_prefill_clear_config_cache", "gqa_prefill_config_block_n",
     "gqa_prefill_selftest_timeout", "gqa_prefill_force_q_tiles",
     "gqa_flash_prefill_splitkv", "gqa_prefill_splitkv_workspace",
-    "gqa_flash_prefill_splitkv_noalloc",
+    "gqa_flash_prefill_splitkv_noalloc", "gqa_flash_prefill_paged",
 ]
 NOALLOC_SCRATCH_BYTES = 32 << 20  # the library's file-scope split-KV scratch (gqa_prefill.h)
 
@@ -76,6 +76,9 @@ def load(path: Optional[str] = None):
     lib.gqa_flash_prefill_debug.restype = ctypes.c_int
     lib.gqa_flash_prefill_splitkv.argtypes = core[:-1] + [ctypes.c_int, vp, ctypes.c_size_t, vp]
     lib.gqa_flash_prefill_splitkv.restype = ctypes.c_int
+    lib.gqa_flash_prefill_paged.argtypes = [vp] * 7 + [ctypes.c_int] * 10 + [
+        ctypes.c_float, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]
+    lib.gqa_flash_prefill_paged.restype = ctypes.c_int
     lib.gqa_flash_prefill_splitkv_noalloc.argtypes = core[:-1] + [ctypes.c_int, vp]
     lib.gqa_flash_prefill_splitkv_noalloc.restype = ctypes.c_int
     lib.gqa_prefill_splitkv_workspace.argtypes = [ctypes.c_int] * 9 + [
@@ -256,6 +259,49 @@ def prefill_splitkv(batch, num_splits=0, workspace=None, out=None, lse=None, wit
                               num_splits=num_splits, window=batch.window, sinks=batch.sinks,
                               smooth_softmax=batch.smooth, out=out, lse=lse, stream=stream,
                               max_seqlen_q=batch.max_seqlen_q)
+    return out, lse
+
+
+def gqa_flash_prefill_paged(q, k_pages, v_pages, cu_seqlens_q, prefix_lens, kv_page_indptr,
+                            kv_page_indices, scale, window=0, sinks=None, smooth_softmax=False,
+                            out=None, lse=None, stream=None, max_seqlen_q=0):
+    """Marshal a paged-KV call (see gqa_prefill.h): k_pages / v_pages are
+    [num_pages, page_size, Hkv, d]; returns ``out``."""
+    for name, t in (("q", q), ("out", out)):
+        if t.dim() != 3 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [rows, heads, d] tensor")
+    for name, t in (("k_pages", k_pages), ("v_pages", v_pages)):
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [pages, page_size, heads, d] tensor")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("prefix_lens", prefix_lens),
+                    ("kv_page_indptr", kv_page_indptr), ("kv_page_indices", kv_page_indices)):
+        if str(t.dtype) != "torch.int32" or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 tensor")
+    total_q, hq, d = q.shape
+    num_pages, page_size, hkv, _ = k_pages.shape
+    rc = load().gqa_flash_prefill_paged(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(cu_seqlens_q), _ptr(prefix_lens),
+        _ptr(kv_page_indptr), _ptr(kv_page_indices), int(kv_page_indices.numel()),
+        int(page_size), int(num_pages), int(prefix_lens.numel()), int(total_q),
+        int(max_seqlen_q), int(hq), int(hkv), int(d), _dtype_code(q), float(scale), int(window),
+        _ptr(sinks), 1 if smooth_softmax else 0, _ptr(out), _ptr(lse), _stream_handle(stream))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_flash_prefill_paged")
+    return out
+
+
+def prefill_paged(paged, out=None, lse=None, with_lse=True, stream=None):
+    """Run one ``workloads.PagedBatch`` already on the GPU.  Returns (out, lse)."""
+    import torch
+    b = paged.batch
+    if out is None:
+        out = torch.empty_like(b.q)
+    if lse is None and with_lse:
+        lse = torch.empty(b.q.shape[:2], dtype=torch.float32, device=b.q.device)
+    gqa_flash_prefill_paged(b.q, paged.k_pages, paged.v_pages, b.cu_seqlens_q, b.prefix_lens,
+                            paged.page_indptr, paged.page_indices, b.scale, window=b.window,
+                            sinks=b.sinks, smooth_softmax=b.smooth, out=out, lse=lse,
+                            stream=stream, max_seqlen_q=b.max_seqlen_q)
     return out, lse
 
 

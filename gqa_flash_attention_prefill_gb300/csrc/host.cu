@@ -159,6 +159,13 @@ struct SplitArgs {
 };
 constexpr int kMaxSplits = 16;
 
+// Paged KV: the page table and the pool geometry (indices == nullptr: the
+// contiguous layout).
+struct KvPaging {
+  const int32_t* indices = nullptr;
+  int page_size = 0, num_pages = 0;
+};
+
 struct SplitLayout {
   size_t o_off, ml_off, hdr_off, bytes;
 };
@@ -339,15 +346,21 @@ int launch_planned(const Plan& pl, const void* q, const void* k, const void* v,
                    const int32_t* kv_indptr, int num_seqs, int total_q, int total_kv, int Hq,
                    int Hkv, int d, int dtype, float scale, int window, const float* sinks,
                    int smooth_softmax, void* out, float* lse, void* stream, int32_t* unit_log,
-                   const SplitArgs& sp = SplitArgs()) {
+                   const SplitArgs& sp = SplitArgs(), const KvPaging& pg = KvPaging()) {
   DeviceInfo di;
   if (device_info(&di) != GQA_OK) return GQA_ERR_CUDA;
 
   PrefillParams p;
   std::memset(&p, 0, sizeof(p));
+  const bool paged = pg.indices != nullptr;
+  const int bn = pl.shape.block_n;
+  // K/V rows the maps cover and rows per box: the pool's page slots in boxes
+  // of min(BN, page_size) rows, or the contiguous rows in boxes of BN.
+  const int kv_rows = paged ? pg.num_pages * pg.page_size : total_kv;
+  const int kv_box = paged ? (pg.page_size < bn ? pg.page_size : bn) : bn;
   int rc = encode_map(&p.tmap_q, q, dtype, d, Hq, total_q, pl.G, pl.rows);
-  if (rc == GQA_OK) rc = encode_map(&p.tmap_k, k, dtype, d, Hkv, total_kv, 1, pl.shape.block_n);
-  if (rc == GQA_OK) rc = encode_map(&p.tmap_v, v, dtype, d, Hkv, total_kv, 1, pl.shape.block_n);
+  if (rc == GQA_OK) rc = encode_map(&p.tmap_k, k, dtype, d, Hkv, kv_rows, 1, kv_box);
+  if (rc == GQA_OK) rc = encode_map(&p.tmap_v, v, dtype, d, Hkv, kv_rows, 1, kv_box);
   if (rc == GQA_OK) rc = encode_map(&p.tmap_o, out, dtype, d, Hq, total_q, pl.G, pl.rows);
   if (rc != GQA_OK) return rc;
   p.cu_seqlens_q = cu_seqlens_q;
@@ -369,6 +382,10 @@ int launch_planned(const Plan& pl, const void* q, const void* k, const void* v,
   p.smooth = smooth_softmax != 0 ? 1 : 0;
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.timeout_ns = timeout_ns();
+  p.kv_page_indices = pg.indices;
+  p.page_size = pg.page_size;
+  p.num_pages = pg.num_pages;
+  p.page_rows = kv_box;
   p.num_splits = sp.num_splits > 1 ? sp.num_splits : 1;
   p.part_o = sp.part_o;
   p.part_ml = sp.part_ml;
@@ -382,7 +399,9 @@ int launch_planned(const Plan& pl, const void* q, const void* k, const void* v,
   const bool bf16 = dtype == GQA_BF16;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (p.num_splits > 1)
+  if (paged)
+    e = launch_paged(p, pl.shape, d, win, bf16, grid, pl.smem_launch, st);
+  else if (p.num_splits > 1)
     e = launch_split(p, pl.shape, d, win, bf16, grid, pl.smem_launch, st);
   else if (d == 64)
     e = launch_d64(p, pl.shape, win, bf16, grid, pl.smem_launch, st);
@@ -563,6 +582,52 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q
                         stream, unit_log, sp);
 }
 
+// Paged KV: the same validation as run(), the pool geometry checks, and a
+// plan whose key tile has a paged instantiation and tiles the pages.
+int run_paged(const void* q, const void* k_pages, const void* v_pages,
+              const int32_t* cu_seqlens_q, const int32_t* prefix_lens,
+              const int32_t* kv_page_indptr, const int32_t* kv_page_indices,
+              int num_page_entries, int page_size, int num_pages, int num_seqs, int total_q,
+              int max_seqlen_q, int Hq, int Hkv, int d, int dtype, float scale, int window,
+              const float* sinks, int smooth_softmax, void* out, float* lse, void* stream) {
+  if (num_seqs < 0 || total_q < 0 || num_page_entries < 0 || max_seqlen_q < 0)
+    return GQA_ERR_INVALID;
+  if (Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return GQA_ERR_INVALID;
+  if (dtype != GQA_F16 && dtype != GQA_BF16) return GQA_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return GQA_ERR_INVALID;
+  if (sinks != nullptr && smooth_softmax != 0) return GQA_ERR_INVALID;
+  if (page_size < 8 || page_size % 8 != 0 || num_pages <= 0 ||
+      (long long)num_pages * page_size >= (1ll << 31))
+    return GQA_ERR_INVALID;
+  if (num_seqs == 0 || total_q == 0) return GQA_OK;  // no work, no launch
+  if (q == nullptr || k_pages == nullptr || v_pages == nullptr || out == nullptr ||
+      cu_seqlens_q == nullptr || prefix_lens == nullptr || kv_page_indptr == nullptr ||
+      kv_page_indices == nullptr || num_page_entries == 0)
+    return GQA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out))
+    return GQA_ERR_INVALID;
+  if (d != 64 && d != 128 && d != 256) return GQA_ERR_UNSUPPORTED;
+  Plan pl;
+  int rc = make_plan(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, &pl);
+  if (rc != GQA_OK) return rc;
+  auto tiles_pages = [&](int bn) { return page_size % bn == 0 || bn % page_size == 0; };
+  if (!split_shape(d, pl.shape.block_n, pl.shape.q_tiles) || !tiles_pages(pl.shape.block_n)) {
+    int bn = 0;
+    for (int cand : {128, 64})
+      if (bn == 0 && split_shape(d, cand, 1) && tiles_pages(cand)) bn = cand;
+    if (bn == 0) return GQA_ERR_UNSUPPORTED;
+    rc = make_plan_bn(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, bn, 1, &pl);
+    if (rc != GQA_OK) return rc;
+  }
+  KvPaging pg;
+  pg.indices = kv_page_indices;
+  pg.page_size = page_size;
+  pg.num_pages = num_pages;
+  return launch_planned(pl, q, k_pages, v_pages, cu_seqlens_q, prefix_lens, kv_page_indptr,
+                        num_seqs, total_q, num_page_entries, Hq, Hkv, d, dtype, scale, window,
+                        sinks, smooth_softmax, out, lse, stream, nullptr, SplitArgs(), pg);
+}
+
 }  // namespace
 
 bool kernel_shape(int d, int block_n, int q_tiles, KernelShape* out) {
@@ -628,6 +693,19 @@ int gqa_flash_prefill_splitkv(const void* q, const void* k, const void* v,
   return gqa::run(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs, total_q, total_kv,
                   max_seqlen_q, Hq, Hkv, d, dtype, scale, window, sinks, smooth_softmax, out, lse,
                   stream, nullptr, num_splits, workspace, workspace_bytes);
+}
+
+int gqa_flash_prefill_paged(const void* q, const void* k_pages, const void* v_pages,
+                            const int32_t* cu_seqlens_q, const int32_t* prefix_lens,
+                            const int32_t* kv_page_indptr, const int32_t* kv_page_indices,
+                            int num_page_entries, int page_size, int num_pages, int num_seqs,
+                            int total_q, int max_seqlen_q, int Hq, int Hkv, int d, int dtype,
+                            float scale, int window, const float* sinks, int smooth_softmax,
+                            void* out, float* lse, void* stream) {
+  return gqa::run_paged(q, k_pages, v_pages, cu_seqlens_q, prefix_lens, kv_page_indptr,
+                        kv_page_indices, num_page_entries, page_size, num_pages, num_seqs,
+                        total_q, max_seqlen_q, Hq, Hkv, d, dtype, scale, window, sinks,
+                        smooth_softmax, out, lse, stream);
 }
 
 int gqa_prefill_splitkv_workspace(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv,

@@ -40,6 +40,9 @@ cudaError_t launch_d256(const PrefillParams& p, const KernelShape& ks, bool win,
 bool split_shape(int d, int block_n, int q_tiles);
 cudaError_t launch_split(const PrefillParams& p, const KernelShape& ks, int d, bool win,
                          bool bf16, int grid, unsigned smem, cudaStream_t st);
+// Paged-KV instantiations (inst_paged.cu), same shapes as split_shape.
+cudaError_t launch_paged(const PrefillParams& p, const KernelShape& ks, int d, bool win,
+                         bool bf16, int grid, unsigned smem, cudaStream_t st);
 
 // Split-KV merge (merge.cu): one 128-thread block per unit, `grid` >= units.
 cudaError_t launch_merge(const PrefillParams& p, int d, bool bf16, int part_rows, int grid,
@@ -57,9 +60,9 @@ struct SmemAttr {
   std::atomic<unsigned> allowed[kMaxDevices];
 };
 
-template <int D, int BN, int NS, bool WIN, bool BF16, int MINB, int QT, bool SPL>
+template <int D, int BN, int NS, bool WIN, bool BF16, int MINB, int QT, bool SPL, bool PAGED>
 cudaError_t launch_one(const PrefillParams& p, int grid, unsigned smem, cudaStream_t st) {
-  auto kern = prefill_kernel<D, BN, NS, WIN, BF16, MINB, QT, SPL>;
+  auto kern = prefill_kernel<D, BN, NS, WIN, BF16, MINB, QT, SPL, PAGED>;
   static SmemAttr attr{};
   if (smem < smem_bytes_for(D, BN, NS, QT)) return cudaErrorInvalidValue;
   int dev = 0;
@@ -75,14 +78,14 @@ cudaError_t launch_one(const PrefillParams& p, int grid, unsigned smem, cudaStre
   return cudaGetLastError();
 }
 
-template <int D, int BN, int NS, int MINB, int QT, bool SPL = false>
+template <int D, int BN, int NS, int MINB, int QT, bool SPL = false, bool PAGED = false>
 cudaError_t launch_variants(const PrefillParams& p, bool win, bool bf16, int grid, unsigned smem,
                             cudaStream_t st) {
   if (win)
-    return bf16 ? launch_one<D, BN, NS, true, true, MINB, QT, SPL>(p, grid, smem, st)
-                : launch_one<D, BN, NS, true, false, MINB, QT, SPL>(p, grid, smem, st);
-  return bf16 ? launch_one<D, BN, NS, false, true, MINB, QT, SPL>(p, grid, smem, st)
-              : launch_one<D, BN, NS, false, false, MINB, QT, SPL>(p, grid, smem, st);
+    return bf16 ? launch_one<D, BN, NS, true, true, MINB, QT, SPL, PAGED>(p, grid, smem, st)
+                : launch_one<D, BN, NS, true, false, MINB, QT, SPL, PAGED>(p, grid, smem, st);
+  return bf16 ? launch_one<D, BN, NS, false, true, MINB, QT, SPL, PAGED>(p, grid, smem, st)
+              : launch_one<D, BN, NS, false, false, MINB, QT, SPL, PAGED>(p, grid, smem, st);
 }
 
 }  // namespace

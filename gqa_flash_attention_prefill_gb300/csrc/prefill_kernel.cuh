@@ -71,6 +71,12 @@ struct PrefillParams {
   float* part_o;      // unnormalised O: [item][d/4][QT*128 rows][4]
   float* part_ml;     // (m in the log2 domain, l) per row: [item][QT*128][2]
   int32_t* part_hdr;  // [0] units; [4 + 4 u ..] (first q row, KV head, valid positions, 0)
+  // Paged KV: K/V are a pool of num_pages pages of page_size tokens; the keys
+  // of sequence b are the pages kv_page_indices[kv_indptr[b] ..] in order, and
+  // tmap_k / tmap_v address the pool as rows page * page_size + slot with
+  // boxes of page_rows = min(BN, page_size) rows.
+  const int32_t* kv_page_indices;
+  int page_size, num_pages, page_rows;
 };
 
 __host__ __device__ constexpr int pow2_cols(int n) {
@@ -183,6 +189,38 @@ __device__ __forceinline__ Unit decode_item(const PrefillParams& p, const SeqTab
   return U;
 }
 
+// Issues the TMA loads of key tile [n0, n0 + BN) of unit U into `dst`
+// (kv_chunk bytes per 64-column chunk, NCH chunks).  Contiguous KV: one box
+// per chunk at row kv_base + n0.  Paged KV: BN / page_rows boxes per chunk,
+// each from the page that holds its first key, looked up in the page table
+// just before its copy (prefetching page numbers a tile ahead measured
+// slower: the K and V lanes share a warp); a box starting past the sequence's
+// last key (masked keys of its last tile) reads the last page, and a page
+// number outside the pool raises GQA_DEV_BAD_METADATA and reads page 0.
+template <bool PAGED, int BN, int NCH>
+__device__ __forceinline__ void load_kv_tile(const PrefillParams& p, const Unit& U, int n0,
+                                             const CUtensorMap* tmap, uint32_t dst,
+                                             uint32_t kv_chunk, uint32_t bar) {
+  if constexpr (!PAGED) {
+    for (int c = 0; c < NCH; ++c)
+      tma_load_3d(dst + c * kv_chunk, tmap, bar, c * 64, U.g, U.kv_base + n0);
+  } else {
+    const int ps = p.page_size, boxr = p.page_rows;
+    const int npg = (U.P + U.E + ps - 1) / ps;  // the sequence's pages
+    for (int sub = 0; sub < BN; sub += boxr) {
+      const int n = n0 + sub;
+      int pg = __ldg(p.kv_page_indices + U.kv_base + min(n / ps, npg - 1));
+      if (pg < 0 || pg >= p.num_pages) {
+        atomicOr(p.status, 2u);  // GQA_DEV_BAD_METADATA
+        pg = 0;
+      }
+      const int row = pg * ps + n % ps;
+      for (int c = 0; c < NCH; ++c)
+        tma_load_3d(dst + c * kv_chunk + (uint32_t)sub * 128u, tmap, bar, c * 64, U.g, row);
+    }
+  }
+}
+
 // k-th unit of this CTA: round k of a snake (boustrophedon) deal over the
 // grid, so that with units ordered by decreasing cost every CTA alternates
 // between the expensive and the cheap end of each round.
@@ -231,9 +269,10 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity,
 }
 
 
-// SPL: split-KV work items writing partials (a separate instantiation, so the
-// unsplit kernel carries none of its code).
-template <int D, int BN, int NS, bool WIN, bool BF16, int MINB, int QT, bool SPL>
+// SPL: split-KV work items writing partials; PAGED: K/V from a page pool.
+// Both are separate instantiations, so the default kernel carries none of
+// their code.
+template <int D, int BN, int NS, bool WIN, bool BF16, int MINB, int QT, bool SPL, bool PAGED>
 __global__ void __launch_bounds__(threads_for(QT), MINB)
     prefill_kernel(const __grid_constant__ PrefillParams p) {
   static_assert(D == 64 || D == 128 || D == 256, "head dim");
@@ -314,8 +353,11 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
     const int P = __ldg(p.prefix_lens + b);
     const int k0 = __ldg(p.kv_indptr + b), k1 = __ldg(p.kv_indptr + b + 1);
     const int E = c1 - c0;
+    // KV rows (contiguous) or pages (paged) of the sequence: exactly P + E keys.
+    const long long kv_need =
+        PAGED ? ((long long)P + E + p.page_size - 1) / p.page_size : (long long)P + E;
     if (E < 0 || P < 0 || c0 < 0 || c1 > p.total_q || k0 < 0 || k1 > p.total_kv ||
-        (long long)k1 - k0 != (long long)P + E)
+        (long long)k1 - k0 != kv_need)
       bad = true;
     else
       local += (E + urows - 1) / urows;
@@ -408,10 +450,8 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
           if (!(ok = wait_bounded(sBar + 8u * (B::kKEmpty + s), ph ^ 1u, abort_flag, p.status, tmo)))
             break;
           mbar_arrive_expect_tx(sBar + 8u * (B::kKFull + s), kKVBytes);
-          const int row = U.kv_base + U.kv_lo + j * BN;
-          for (int c = 0; c < NCH; ++c)
-            tma_load_3d(sK + s * kKVBytes + c * kKVChunk, &p.tmap_k, sBar + 8u * (B::kKFull + s),
-                        c * 64, U.g, row);
+          load_kv_tile<PAGED, BN, NCH>(p, U, U.kv_lo + j * BN, &p.tmap_k, sK + s * kKVBytes,
+                                       kKVChunk, sBar + 8u * (B::kKFull + s));
           ++nk[s];
         }
         if (!ok) break;
@@ -439,10 +479,8 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
           if (!(ok = wait_bounded(sBar + 8u * (B::kVEmpty + s), ph ^ 1u, abort_flag, p.status, tmo)))
             break;
           mbar_arrive_expect_tx(sBar + 8u * (B::kVFull + s), kKVBytes);
-          const int row = U.kv_base + U.kv_lo + j * BN;
-          for (int c = 0; c < NCH; ++c)
-            tma_load_3d(sV + s * kKVBytes + c * kKVChunk, &p.tmap_v, sBar + 8u * (B::kVFull + s),
-                        c * 64, U.g, row);
+          load_kv_tile<PAGED, BN, NCH>(p, U, U.kv_lo + j * BN, &p.tmap_v, sV + s * kKVBytes,
+                                       kKVChunk, sBar + 8u * (B::kVFull + s));
           ++nv[s];
         }
       }

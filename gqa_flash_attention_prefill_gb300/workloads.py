@@ -239,3 +239,48 @@ def decode(num_seqs: int = 128, min_prefix: int = 1024, max_prefix: int = 16384,
     b = make_batch(pre, [1] * num_seqs, hq, hkv, d, dtype, window=window, sink_mode=sink_mode,
                    seed=seed, name=f"decode-{num_seqs}-h{hq}/{hkv}-d{d}-{dtype}-w{window}")
     return window_bounded(b, window) if (window_bounded_layout and window > 0) else b
+
+
+@dataclass
+class PagedBatch:
+    """A Batch whose K/V also live in a page pool: page p of the pool holds
+    page_size consecutive keys of one sequence; the pages are placed in a
+    seeded random order, and unused pool pages hold noise."""
+    batch: Batch
+    k_pages: torch.Tensor    # [num_pages, page_size, Hkv, d]
+    v_pages: torch.Tensor
+    page_indptr: torch.Tensor   # int32 [B+1]
+    page_indices: torch.Tensor  # int32 [entries]
+    page_size: int
+
+    def to(self, device) -> "PagedBatch":
+        return PagedBatch(self.batch.to(device), self.k_pages.to(device),
+                          self.v_pages.to(device), self.page_indptr.to(device),
+                          self.page_indices.to(device), self.page_size)
+
+
+def paged(batch: Batch, page_size: int, spare_pages: int = 3, seed: int = 0) -> PagedBatch:
+    """Lay a contiguous batch's K/V out as a shuffled page pool (the keys and
+    their order per sequence are unchanged: only the placement differs)."""
+    gen = torch.Generator().manual_seed(int(seed) * 31337 + page_size)
+    kvp = batch.kv_indptr.tolist()
+    counts = [-(-(kvp[b + 1] - kvp[b]) // page_size) for b in range(batch.num_seqs)]
+    n_used = sum(counts)
+    num_pages = n_used + spare_pages
+    place = torch.randperm(num_pages, generator=gen)[:n_used]  # pool page of each used page
+    hkv, d = batch.k.shape[1], batch.k.shape[2]
+    k_pages = torch.randn(num_pages, page_size, hkv, d, generator=gen).to(batch.k.dtype)
+    v_pages = torch.randn(num_pages, page_size, hkv, d, generator=gen).to(batch.v.dtype)
+    indptr, indices, u = [0], [], 0
+    for b in range(batch.num_seqs):
+        for pg in range(counts[b]):
+            page = int(place[u])
+            u += 1
+            lo = kvp[b] + pg * page_size
+            hi = min(lo + page_size, kvp[b + 1])
+            k_pages[page, : hi - lo] = batch.k[lo:hi]
+            v_pages[page, : hi - lo] = batch.v[lo:hi]
+            indices.append(page)
+        indptr.append(len(indices))
+    return PagedBatch(batch, k_pages, v_pages, torch.tensor(indptr, dtype=torch.int32),
+                      torch.tensor(indices, dtype=torch.int32), page_size)

@@ -119,6 +119,45 @@ GQA_API int gqa_flash_prefill(const void* q, const void* k, const void* v,
                       int smooth_softmax, void* out, float* lse, void* stream);
 
 /*
+ * gqa_flash_prefill_paged -- the same operation as gqa_flash_prefill with K
+ * and V held in a page pool, the way serving stacks hand over a cached prefix
+ * (the kv_indices / window_kv_indices page tables of SGLang PR #34468).
+ *
+ *   k_pages, v_pages   device [num_pages, page_size, Hkv, d], q's dtype,
+ *                      16-byte aligned.
+ *   kv_page_indptr     device int32 [num_seqs + 1]: the pages of sequence b
+ *                      are kv_page_indices[kv_page_indptr[b] ..
+ *                      kv_page_indptr[b+1]), in key order; there must be
+ *                      exactly ceil((prefix_lens[b] + E_b) / page_size).
+ *   kv_page_indices    device int32 [num_page_entries], page numbers in
+ *                      [0, num_pages).
+ *   page_size          tokens per page: a multiple of 8 that divides, or is
+ *                      divided by, the kernel's key tile of 64 or 128 (every
+ *                      power of two from 8 qualifies); else GQA_ERR_UNSUPPORTED.
+ *
+ * Key j of sequence b is slot j % page_size of page
+ * kv_page_indices[kv_page_indptr[b] + j / page_size]; prefix_lens[b] counts
+ * the prefix keys the pages hold (the whole prefix, or its last
+ * min(prefix, window) keys for a window-bounded table), exactly as the
+ * contiguous layout.  Other arguments, layouts and return codes as
+ * gqa_flash_prefill.  A page count that disagrees with the lengths is
+ * reported through GQA_DEV_BAD_METADATA with nothing written; a page number
+ * outside the pool raises GQA_DEV_BAD_METADATA as well, and the rows of that
+ * call are then unspecified.
+ */
+GQA_API int gqa_flash_prefill_paged(const void* q, const void* k_pages,
+                                    const void* v_pages, const int32_t* cu_seqlens_q,
+                                    const int32_t* prefix_lens,
+                                    const int32_t* kv_page_indptr,
+                                    const int32_t* kv_page_indices,
+                                    int num_page_entries, int page_size,
+                                    int num_pages, int num_seqs, int total_q,
+                                    int max_seqlen_q, int Hq, int Hkv, int d,
+                                    int dtype, float scale, int window,
+                                    const float* sinks, int smooth_softmax,
+                                    void* out, float* lse, void* stream);
+
+/*
  * gqa_flash_prefill_splitkv -- the same operation as gqa_flash_prefill, with
  * each work unit's key tiles divided into num_splits contiguous ranges
  * processed by separate CTAs, for calls whose units would not fill the GPU
