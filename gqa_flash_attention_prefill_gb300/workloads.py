@@ -259,15 +259,18 @@ class PagedBatch:
                           self.page_indices.to(device), self.page_size)
 
 
-def paged(batch: Batch, page_size: int, spare_pages: int = 3, seed: int = 0) -> PagedBatch:
-    """Lay a contiguous batch's K/V out as a shuffled page pool (the keys and
-    their order per sequence are unchanged: only the placement differs)."""
+def paged(batch: Batch, page_size: int, spare_pages: int = 3, seed: int = 0,
+          shuffle: bool = True) -> PagedBatch:
+    """Lay a contiguous batch's K/V out as a page pool, the pages placed in a
+    seeded random order (shuffle) or in order (the keys and their order per
+    sequence are unchanged: only the placement differs)."""
     gen = torch.Generator().manual_seed(int(seed) * 31337 + page_size)
     kvp = batch.kv_indptr.tolist()
     counts = [-(-(kvp[b + 1] - kvp[b]) // page_size) for b in range(batch.num_seqs)]
     n_used = sum(counts)
     num_pages = n_used + spare_pages
-    place = torch.randperm(num_pages, generator=gen)[:n_used]  # pool page of each used page
+    order = torch.randperm(num_pages, generator=gen) if shuffle else torch.arange(num_pages)
+    place = order[:n_used]  # pool page of each used page
     hkv, d = batch.k.shape[1], batch.k.shape[2]
     k_pages = torch.randn(num_pages, page_size, hkv, d, generator=gen).to(batch.k.dtype)
     v_pages = torch.randn(num_pages, page_size, hkv, d, generator=gen).to(batch.v.dtype)
