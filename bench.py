@@ -352,6 +352,12 @@ def run_workload(args, rank, world):
         desc = ("ragged varlen: 16 sequences, prefixes U[0,16384], extends U[1,8192], 64/8, d 64, "
                 "bf16, window 128, sinks")
         tokens = b.total_q
+    elif args.workload == "ragged_full":
+        b = W.ragged(hq=64, hkv=8, d=64, dtype="bf16", window=0, sink_mode="head", seed=4)
+        calls = [b.to(dev)]
+        desc = ("ragged varlen, full causal: 16 sequences, prefixes U[0,16384], extends "
+                "U[1,8192], 64/8, d 64, bf16, sinks")
+        tokens = b.total_q
     elif args.workload == "decode":
         b = W.decode(num_seqs=128, min_prefix=1024, max_prefix=16384, window=128,
                      sink_mode="head", seed=6,
@@ -449,6 +455,12 @@ def run_workload(args, rank, world):
         line["roofline"] = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                             "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                             "traffic": None, "algorithmic_bytes": nbytes}
+    if args.workload == "ragged_full":
+        # Tensor-bound: useful flops over the measured dense bf16 peak (burst; one call).
+        line["roofline"] = {"bound": "tensor", "achieved": round(value / world, 1),
+                            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                            "frac": round(value / world / peaks["bf16_tflops"], 4),
+                            "traffic": None}
     return line
 
 
@@ -558,8 +570,8 @@ def main():
                     help="CPU work of the oracle baseline sample (rank 0, N=1)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="layer_pair",
-                    choices=["layer_pair", "chunked_prefix", "oss20b_16k", "ragged", "short_chunk",
-                             "decode"],
+                    choices=["layer_pair", "chunked_prefix", "oss20b_16k", "ragged", "ragged_full",
+                             "short_chunk", "decode"],
                     help="layer_pair is the headline configuration; the others are "
                          "supplementary measurements")
     ap.add_argument("--layout", default="window-bounded", choices=["window-bounded", "full-prefix"],
