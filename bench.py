@@ -232,6 +232,19 @@ def run_ours(args, rank, world):
     full_ms = statistics.mean(t_full)
     achieved = flops[0] / (full_ms * 1e-3) / 1e12
 
+    # The same launches without the L2 flush (the layer pair's 75 MB of
+    # operands can then stay in the 129 MB L2 between steps): reported beside
+    # the flushed figure, which remains `value`.
+    n_warm = max(3, min(args.steps, 200))
+    ev_w = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_warm)]
+    for i in range(n_warm):
+        ev_w[i][0].record(stream)
+        pkg.prefill(layers[0], out=outs[0], lse=lses[0], stream=stream)
+        pkg.prefill(layers[1], out=outs[1], lse=lses[1], stream=stream)
+        ev_w[i][1].record(stream)
+    torch.cuda.synchronize()
+    warm_ms = dist_max(statistics.mean(e[0].elapsed_time(e[1]) for e in ev_w), world)
+
     # End to end through the C ABI from pinned host buffers: per step, copy
     # this step's inputs host->device, run both layers, read the outputs back.
     host = []
@@ -317,8 +330,80 @@ def run_ours(args, rank, world):
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
         "timed_wall_s": round(t_wall1 - t_wall0, 3),
+        "warm_l2": {"ms_per_step": round(warm_ms, 5), "steps": n_warm,
+                    "value": round(world * sum(flops) / (warm_ms * 1e-3) / 1e12, 2),
+                    "unit": UNIT, "note": "no L2 flush between steps; not the headline"},
     }
     return line
+
+
+def run_ragged_grid(args, rank, world):
+    """Throughput per cell of a grid over head counts, head dims and windows,
+    on one ragged batch shape (16 sequences, prefixes U[0,16384], extends
+    U[1,8192], seed 4): one call per cell, L2 flushed before each timed call.
+    The inputs are generated on the GPU from a seeded CUDA generator."""
+    import torch
+    import gqa_flash_attention_prefill_gb300 as pkg
+    from gqa_flash_attention_prefill_gb300 import workloads as W
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    pkg.load()
+    gen = torch.Generator().manual_seed(4 * 7919 + 17)  # the lengths of workloads.ragged(seed=4)
+    pre = torch.randint(0, 16384 + 1, (16,), generator=gen).tolist()
+    ext = torch.randint(1, 8192 + 1, (16,), generator=gen).tolist()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    peaks = load_peaks()
+    steps = max(3, min(args.steps, args.grid_steps))
+    cells, tot_flops, tot_ms, launches = [], 0.0, 0.0, 0
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for hq, hkv in ((64, 8), (32, 4)):
+            for d in (64, 128, 256):
+                for window in (0, 128):
+                    b = W.make_batch(pre, ext, hq, hkv, d, "bf16", window=window,
+                                     sink_mode="head", seed=4, device="cuda",
+                                     name=f"grid-{hq}/{hkv}-d{d}-w{window}")
+                    out = torch.empty_like(b.q)
+                    lse = torch.empty(b.q.shape[:2], dtype=torch.float32, device="cuda")
+                    for _ in range(args.warmup):
+                        flush.fill_(1.0)
+                        pkg.prefill(b, out=out, lse=lse, stream=stream)
+                    ts = []
+                    for i in range(steps):
+                        flush.fill_(float(i))
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        pkg.prefill(b, out=out, lse=lse, stream=stream)
+                        e1.record(stream)
+                        e1.synchronize()
+                        ts.append(e0.elapsed_time(e1))
+                    launches += steps
+                    if pkg.get_device_status() != 0:
+                        raise RuntimeError("device status word raised in " + b.name)
+                    ms = dist_max(statistics.median(ts), world)
+                    fl = 4.0 * d * hq * useful_pairs(pre, ext, window)
+                    tf = world * fl / (ms * 1e-3) / 1e12
+                    cells.append({"hq": hq, "hkv": hkv, "d": d, "window": window, "ms": round(ms, 4),
+                                  "tflops": round(tf, 1),
+                                  "pct_of_bf16_peak": round(100.0 * tf / (world * peaks["bf16_tflops"]), 1)})
+                    tot_flops += fl
+                    tot_ms += ms
+                    del b, out, lse
+        clk.mark(t0, time.perf_counter())
+    value = world * tot_flops / (tot_ms * 1e-3) / 1e12
+    return {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": round(tot_ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) Q/K/V and sinks, generated on the GPU)",
+            "config": {"workload": "ragged grid: 16 sequences, prefixes U[0,16384], extends "
+                                   "U[1,8192]; {64/8, 32/4} x d {64, 128, 256} x window "
+                                   "{none, 128}; bf16, per-head sinks; one call per cell, "
+                                   "median of the steps; value = all cells' flops / summed times",
+                       "l2": "flushed before every timed call (256 MiB write)"},
+            "cells": cells, "gpu_launches": launches, "clocks": clk.summary()}
 
 
 def run_workload(args, rank, world):
@@ -571,7 +656,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="layer_pair",
                     choices=["layer_pair", "chunked_prefix", "oss20b_16k", "ragged", "ragged_full",
-                             "short_chunk", "decode"],
+                             "ragged_grid", "short_chunk", "decode"],
                     help="layer_pair is the headline configuration; the others are "
                          "supplementary measurements")
     ap.add_argument("--layout", default="window-bounded", choices=["window-bounded", "full-prefix"],
@@ -579,6 +664,8 @@ def main():
     ap.add_argument("--paged", type=int, default=0,
                     help="supplementary workloads: K/V as a page pool with this page size "
                          "(0: contiguous)")
+    ap.add_argument("--grid-steps", type=int, default=10,
+                    help="ragged_grid: timed calls per cell (capped by --steps)")
     ap.add_argument("--splits", type=int, default=-1,
                     help="supplementary workloads: -1 the plain entry point; 0 split-KV with "
                          "the library's split count; k >= 1 split-KV with k splits")
@@ -588,6 +675,8 @@ def main():
     rank, world = dist_setup()
     if args.impl == "reference":
         line = run_reference(args, rank, world)
+    elif args.workload == "ragged_grid":
+        line = run_ragged_grid(args, rank, world)
     elif args.workload != "layer_pair":
         line = run_workload(args, rank, world)
     else:
