@@ -56,10 +56,17 @@ def load_peaks():
             "source": "fallback"}
 
 
+# The sources that define the roofline kernel (the d=64 single-tile prefill
+# kernel) and its launch: the split-KV merge, the paged and split
+# instantiations and the other head dims do not change it.
+ROOFLINE_KERNEL_SOURCES = ("host.cu", "inst_d64.cu", "launch.h", "prefill_kernel.cuh", "ptx.cuh",
+                           "tile_math.cuh")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gqa_flash_attention_prefill_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in ROOFLINE_KERNEL_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]

@@ -31,69 +31,77 @@ struct MergeParams {
   int num_splits, Hq, G, rows, part_rows, smooth;
 };
 
+// Columns per thread, as float4 groups: a thread merges one row's kColGroup
+// float4 columns (16 values), so a unit's rows spread over D / 16 blocks.
+constexpr int kColGroup = 4;
+
+// Block = the 128 rows of one partial query tile for one group of 16 output
+// columns (thread = row, so every partial load of a warp is 32 consecutive
+// float4s).  Grid = units x query tiles per unit x column groups; blocks past
+// the units the split kernel recorded return at once.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ MergeParams mp) {
-  const int unit = blockIdx.x;
+  constexpr int kGroups = D / 4 / kColGroup;
+  const int grp = blockIdx.x % kGroups;
+  const int tile = blockIdx.x / kGroups;
+  const int tiles_per_unit = mp.part_rows / 128;
+  const int unit = tile / tiles_per_unit;
   if (unit >= mp.part_hdr[0]) return;
   const int32_t* hd = mp.part_hdr + 4 + 4 * (size_t)unit;
   const int row0 = hd[0], g = hd[1], nvalid = hd[2];
   const int S = mp.num_splits;
   const float2* ml = reinterpret_cast<const float2*>(mp.part_ml);
   const float4* po = reinterpret_cast<const float4*>(mp.part_o);
-  for (int rr = threadIdx.x; rr < mp.part_rows; rr += blockDim.x) {
-    const int r = rr % 128;
-    const int off = (rr / 128) * mp.rows + r / mp.G;  // position inside the unit
-    if (off >= nvalid) continue;
-    const int h = g * mp.G + r % mp.G;
-    const size_t orow = (size_t)(row0 + off) * mp.Hq + h;
-    uint16_t* op = reinterpret_cast<uint16_t*>(mp.out) + orow * D;
-    float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, ml[((size_t)unit * S + s) * mp.part_rows + rr].x);
-    if (M == -INFINITY) {  // no key reached this row in any split
-      uint4* dst = reinterpret_cast<uint4*>(op);
-      for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
-      if (mp.lse != nullptr) mp.lse[orow] = -INFINITY;
-      continue;
-    }
-    const bool has_x = (mp.sinks != nullptr) || (mp.smooth != 0);
-    const float ms = mp.sinks != nullptr ? mp.sinks[h] * kLog2e : 0.f;
-    const float mf = has_x ? fmaxf(M, ms) : M;
-    float den = has_x ? ex2(ms - mf) : 0.f;
-    for (int s = 0; s < S; ++s) {
-      const float2 v = ml[((size_t)unit * S + s) * mp.part_rows + rr];
-      if (v.x != -INFINITY) den += v.y * ex2(v.x - mf);
-    }
-    den = fmaxf(den, 1e-30f);
-    const float inv = 1.f / den;
-#pragma unroll 1
-    for (int c0 = 0; c0 < D / 4; c0 += 16) {  // 64 columns at a time
-      float4 acc[16];
+  const int rr = (tile % tiles_per_unit) * 128 + threadIdx.x;  // partial row
+  const int r = threadIdx.x;
+  const int off = (rr / 128) * mp.rows + r / mp.G;  // position inside the unit
+  if (off >= nvalid) return;
+  const int h = g * mp.G + r % mp.G;
+  const size_t orow = (size_t)(row0 + off) * mp.Hq + h;
+  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(mp.out) + orow * D +
+                                        grp * kColGroup * 4);
+  float M = -INFINITY;
+  for (int s = 0; s < S; ++s) M = fmaxf(M, ml[((size_t)unit * S + s) * mp.part_rows + rr].x);
+  if (M == -INFINITY) {  // no key reached this row in any split
 #pragma unroll
-      for (int i = 0; i < 16; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s = 0; s < S; ++s) {
-        const size_t item = (size_t)unit * S + s;
-        const float m_s = ml[item * mp.part_rows + rr].x;
-        if (m_s == -INFINITY) continue;  // an empty split carries no O
-        const float w = ex2(m_s - mf) * inv;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float4 o = po[(item * (D / 4) + c0 + i) * mp.part_rows + rr];
-          acc[i].x += w * o.x;
-          acc[i].y += w * o.y;
-          acc[i].z += w * o.z;
-          acc[i].w += w * o.w;
-        }
-      }
-      uint4* dst = reinterpret_cast<uint4*>(op + c0 * 4);
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        dst[i] = make_uint4(pack2<BF16>(acc[2 * i].x, acc[2 * i].y),
-                            pack2<BF16>(acc[2 * i].z, acc[2 * i].w),
-                            pack2<BF16>(acc[2 * i + 1].x, acc[2 * i + 1].y),
-                            pack2<BF16>(acc[2 * i + 1].z, acc[2 * i + 1].w));
-    }
-    if (mp.lse != nullptr) mp.lse[orow] = (mf + log2f(den)) * kLn2;
+    for (int i = 0; i < kColGroup / 2; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (grp == 0 && mp.lse != nullptr) mp.lse[orow] = -INFINITY;
+    return;
   }
+  const bool has_x = (mp.sinks != nullptr) || (mp.smooth != 0);
+  const float ms = mp.sinks != nullptr ? mp.sinks[h] * kLog2e : 0.f;
+  const float mf = has_x ? fmaxf(M, ms) : M;
+  float den = has_x ? ex2(ms - mf) : 0.f;
+  for (int s = 0; s < S; ++s) {
+    const float2 v = ml[((size_t)unit * S + s) * mp.part_rows + rr];
+    if (v.x != -INFINITY) den += v.y * ex2(v.x - mf);
+  }
+  den = fmaxf(den, 1e-30f);
+  const float inv = 1.f / den;
+  float4 acc[kColGroup];
+#pragma unroll
+  for (int i = 0; i < kColGroup; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < S; ++s) {
+    const size_t item = (size_t)unit * S + s;
+    const float m_s = ml[item * mp.part_rows + rr].x;
+    if (m_s == -INFINITY) continue;  // an empty split carries no O
+    const float w = ex2(m_s - mf) * inv;
+#pragma unroll
+    for (int i = 0; i < kColGroup; ++i) {
+      const float4 o = po[(item * (D / 4) + grp * kColGroup + i) * mp.part_rows + rr];
+      acc[i].x += w * o.x;
+      acc[i].y += w * o.y;
+      acc[i].z += w * o.z;
+      acc[i].w += w * o.w;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kColGroup / 2; ++i)
+    dst[i] = make_uint4(pack2<BF16>(acc[2 * i].x, acc[2 * i].y),
+                        pack2<BF16>(acc[2 * i].z, acc[2 * i].w),
+                        pack2<BF16>(acc[2 * i + 1].x, acc[2 * i + 1].y),
+                        pack2<BF16>(acc[2 * i + 1].z, acc[2 * i + 1].w));
+  if (grp == 0 && mp.lse != nullptr) mp.lse[orow] = (mf + log2f(den)) * kLn2;
 }
 
 template <int D>
@@ -123,9 +131,13 @@ cudaError_t launch_merge(const PrefillParams& p, int d, bool bf16, int part_rows
   mp.part_rows = part_rows;
   mp.smooth = p.smooth;
   if (grid < 1) return cudaSuccess;
-  if (d == 64) return launch_merge_d<64>(mp, bf16, grid, st);
-  if (d == 128) return launch_merge_d<128>(mp, bf16, grid, st);
-  if (d == 256) return launch_merge_d<256>(mp, bf16, grid, st);
+  // Blocks: the units, times the 128-row query tiles of each, times the
+  // column groups of a row.
+  const long long blocks = (long long)grid * (part_rows / 128) * (d / 4 / kColGroup);
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (d == 64) return launch_merge_d<64>(mp, bf16, (int)blocks, st);
+  if (d == 128) return launch_merge_d<128>(mp, bf16, (int)blocks, st);
+  if (d == 256) return launch_merge_d<256>(mp, bf16, (int)blocks, st);
   return cudaErrorInvalidValue;
 }
 
