@@ -34,6 +34,8 @@ struct MergeParams {
 // Columns per thread, as float4 groups: a thread merges one row's kColGroup
 // float4 columns (16 values), so a unit's rows spread over D / 16 blocks.
 constexpr int kColGroup = 4;
+// The largest split count the library accepts.
+constexpr int kMaxMergeSplits = 16;
 
 // Block = the 128 rows of one partial query tile for one group of 16 output
 // columns (thread = row, so every partial load of a warp is 32 consecutive
@@ -60,8 +62,17 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Merg
   const size_t orow = (size_t)(row0 + off) * mp.Hq + h;
   uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(mp.out) + orow * D +
                                         grp * kColGroup * 4);
+  // Every split's (m, l) of this row in one pass (independent loads).
+  float2 mlv[kMaxMergeSplits];
   float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, ml[((size_t)unit * S + s) * mp.part_rows + rr].x);
+#pragma unroll
+  for (int s = 0; s < kMaxMergeSplits; ++s) {
+    mlv[s] = make_float2(-INFINITY, 0.f);
+    if (s < S) {
+      mlv[s] = ml[((size_t)unit * S + s) * mp.part_rows + rr];
+      M = fmaxf(M, mlv[s].x);
+    }
+  }
   if (M == -INFINITY) {  // no key reached this row in any split
 #pragma unroll
     for (int i = 0; i < kColGroup / 2; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -72,27 +83,28 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Merg
   const float ms = mp.sinks != nullptr ? mp.sinks[h] * kLog2e : 0.f;
   const float mf = has_x ? fmaxf(M, ms) : M;
   float den = has_x ? ex2(ms - mf) : 0.f;
-  for (int s = 0; s < S; ++s) {
-    const float2 v = ml[((size_t)unit * S + s) * mp.part_rows + rr];
-    if (v.x != -INFINITY) den += v.y * ex2(v.x - mf);
-  }
+#pragma unroll
+  for (int s = 0; s < kMaxMergeSplits; ++s)
+    if (s < S && mlv[s].x != -INFINITY) den += mlv[s].y * ex2(mlv[s].x - mf);
   den = fmaxf(den, 1e-30f);
   const float inv = 1.f / den;
   float4 acc[kColGroup];
 #pragma unroll
   for (int i = 0; i < kColGroup; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < S; ++s) {
-    const size_t item = (size_t)unit * S + s;
-    const float m_s = ml[item * mp.part_rows + rr].x;
-    if (m_s == -INFINITY) continue;  // an empty split carries no O
-    const float w = ex2(m_s - mf) * inv;
 #pragma unroll
-    for (int i = 0; i < kColGroup; ++i) {
-      const float4 o = po[(item * (D / 4) + grp * kColGroup + i) * mp.part_rows + rr];
-      acc[i].x += w * o.x;
-      acc[i].y += w * o.y;
-      acc[i].z += w * o.z;
-      acc[i].w += w * o.w;
+  for (int s = 0; s < kMaxMergeSplits; ++s) {
+    // An empty split (m = -inf) wrote no O: its partial is not read.
+    if (s < S && mlv[s].x != -INFINITY) {
+      const size_t item = (size_t)unit * S + s;
+      const float w = ex2(mlv[s].x - mf) * inv;
+#pragma unroll
+      for (int i = 0; i < kColGroup; ++i) {
+        const float4 o = po[(item * (D / 4) + grp * kColGroup + i) * mp.part_rows + rr];
+        acc[i].x += w * o.x;
+        acc[i].y += w * o.y;
+        acc[i].z += w * o.z;
+        acc[i].w += w * o.w;
+      }
     }
   }
 #pragma unroll
@@ -131,6 +143,7 @@ cudaError_t launch_merge(const PrefillParams& p, int d, bool bf16, int part_rows
   mp.part_rows = part_rows;
   mp.smooth = p.smooth;
   if (grid < 1) return cudaSuccess;
+  if (p.num_splits > kMaxMergeSplits) return cudaErrorInvalidValue;
   // Blocks: the units, times the 128-row query tiles of each, times the
   // column groups of a row.
   const long long blocks = (long long)grid * (part_rows / 128) * (d / 4 / kColGroup);
