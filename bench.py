@@ -624,8 +624,9 @@ def run_reference(args, rank, world):
     oracle.build()
     layers_cpu = W.layer_pair(seq=args.seq, seed=1)
     layers64 = oracle_inputs(layers_cpu)
-    # About 150 s of oracle work in total, however many steps are asked for.
-    per_step_s = max(0.005, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    # About --ref-seconds (150 s by default) of oracle work in total, however
+    # many steps are asked for.
+    per_step_s = max(0.005, min(5.0, args.ref_seconds / max(1, args.steps + args.warmup)))
     rows = size_oracle_sample(layers64, per_step_s)
     for i in range(args.warmup):
         oracle_sample_run(layers64, rows, offset=i)
@@ -661,6 +662,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="CPU work of the oracle baseline sample (rank 0, N=1)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=150.0,
+                    help="--impl reference: total CPU seconds of oracle work over all steps")
     ap.add_argument("--workload", default="layer_pair",
                     choices=["layer_pair", "chunked_prefix", "oss20b_16k", "ragged", "ragged_full",
                              "ragged_grid", "short_chunk", "decode"],
