@@ -57,6 +57,17 @@ def test_split_head_dims(pkg, d, window):
     check(pkg, b, 4)
 
 
+@pytest.mark.parametrize("d,dtype,sink_mode", [(128, "f16", "smooth"), (256, "bf16", "head")])
+@pytest.mark.parametrize("num_splits", [7, 16])
+@pytest.mark.parametrize("window", [0, 37])
+def test_split_wide_heads_many_splits(pkg, d, dtype, sink_mode, num_splits, window):
+    """Head dims whose merge spreads a row over 8 or 16 column groups, with
+    more splits than some units have tiles (empty splits)."""
+    b = W.make_batch([900, 0, 64], [40, 150, 9], 16, 4, d, dtype, window=window,
+                     sink_mode=sink_mode, seed=d + num_splits + window)
+    check(pkg, b, num_splits)
+
+
 def test_split_short_chunk_long_prefix_auto(pkg):
     """The case split-KV exists for: a 48-query chunk over a 5000-token prefix
     (24 units on a GPU with hundreds of CTA slots)."""
