@@ -192,11 +192,12 @@ __device__ __forceinline__ Unit decode_item(const PrefillParams& p, const SeqTab
 // Issues the TMA loads of key tile [n0, n0 + BN) of unit U into `dst`
 // (kv_chunk bytes per 64-column chunk, NCH chunks).  Contiguous KV: one box
 // per chunk at row kv_base + n0.  Paged KV: BN / page_rows boxes per chunk,
-// each from the page that holds its first key, looked up in the page table
-// just before its copy (prefetching page numbers a tile ahead measured
-// slower: the K and V lanes share a warp); a box starting past the sequence's
-// last key (masked keys of its last tile) reads the last page, and a page
-// number outside the pool raises GQA_DEV_BAD_METADATA and reads page 0.
+// each from the page that holds its first key.  The tile's page numbers are
+// read from the page table just before its copies, all of them before the
+// first copy (prefetching page numbers a tile ahead measured slower: the K
+// and V lanes share a warp); a box starting past the sequence's last key
+// (masked keys of its last tile) reads the last page, and a page number
+// outside the pool raises GQA_DEV_BAD_METADATA and reads page 0.
 template <bool PAGED, int BN, int NCH>
 __device__ __forceinline__ void load_kv_tile(const PrefillParams& p, const Unit& U, int n0,
                                              const CUtensorMap* tmap, uint32_t dst,
@@ -207,14 +208,34 @@ __device__ __forceinline__ void load_kv_tile(const PrefillParams& p, const Unit&
   } else {
     const int ps = p.page_size, boxr = p.page_rows;
     const int npg = (U.P + U.E + ps - 1) / ps;  // the sequence's pages
-    for (int sub = 0; sub < BN; sub += boxr) {
-      const int n = n0 + sub;
-      int pg = __ldg(p.kv_page_indices + U.kv_base + min(n / ps, npg - 1));
+    if (boxr >= BN) {  // one box (page_size >= BN): one lookup
+      int pg = __ldg(p.kv_page_indices + U.kv_base + min(n0 / ps, npg - 1));
       if (pg < 0 || pg >= p.num_pages) {
         atomicOr(p.status, 2u);  // GQA_DEV_BAD_METADATA
         pg = 0;
       }
-      const int row = pg * ps + n % ps;
+      for (int c = 0; c < NCH; ++c)
+        tma_load_3d(dst + c * kv_chunk, tmap, bar, c * 64, U.g, pg * ps + n0 % ps);
+      return;
+    }
+    // All the tile's page numbers are loaded before the first copy, so their
+    // latencies overlap (a box is at least 8 rows: at most BN / 8 boxes).
+    constexpr int kMaxBoxes = BN / 8;
+    int pgs[kMaxBoxes];
+#pragma unroll
+    for (int i = 0; i < kMaxBoxes; ++i)
+      if (i * boxr < BN)
+        pgs[i] = __ldg(p.kv_page_indices + U.kv_base + min((n0 + i * boxr) / ps, npg - 1));
+#pragma unroll
+    for (int i = 0; i < kMaxBoxes; ++i) {
+      const int sub = i * boxr;
+      if (sub >= BN) break;
+      int pg = pgs[i];
+      if (pg < 0 || pg >= p.num_pages) {
+        atomicOr(p.status, 2u);  // GQA_DEV_BAD_METADATA
+        pg = 0;
+      }
+      const int row = pg * ps + (n0 + sub) % ps;
       for (int c = 0; c < NCH; ++c)
         tma_load_3d(dst + c * kv_chunk + (uint32_t)sub * 128u, tmap, bar, c * 64, U.g, row);
     }
