@@ -31,18 +31,22 @@ struct MergeParams {
   int num_splits, Hq, G, rows, part_rows, smooth;
 };
 
-// Columns per thread, as float4 groups: a thread merges one row's kColGroup
-// float4 columns (16 values), so a unit's rows spread over D / 16 blocks.
-constexpr int kColGroup = 4;
+// Columns per thread, as float4 groups: a thread merges one row's
+// col_group<D>() float4 columns (8 values at d = 64, else 16), so a unit's
+// rows spread over d / 8 or d / 16 blocks; the smaller group at d = 64 gives
+// the short merges there twice the blocks (4-sequence decode 31.4 -> 28.8 us).
+template <int D>
+__host__ __device__ constexpr int col_group() { return D == 64 ? 2 : 4; }
 // The largest split count the library accepts.
 constexpr int kMaxMergeSplits = 16;
 
-// Block = the 128 rows of one partial query tile for one group of 16 output
+// Block = the 128 rows of one partial query tile for one group of output
 // columns (thread = row, so every partial load of a warp is 32 consecutive
 // float4s).  Grid = units x query tiles per unit x column groups; blocks past
 // the units the split kernel recorded return at once.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ MergeParams mp) {
+  constexpr int kColGroup = col_group<D>();
   constexpr int kGroups = D / 4 / kColGroup;
   const int grp = blockIdx.x % kGroups;
   const int tile = blockIdx.x / kGroups;
@@ -146,7 +150,8 @@ cudaError_t launch_merge(const PrefillParams& p, int d, bool bf16, int part_rows
   if (p.num_splits > kMaxMergeSplits) return cudaErrorInvalidValue;
   // Blocks: the units, times the 128-row query tiles of each, times the
   // column groups of a row.
-  const long long blocks = (long long)grid * (part_rows / 128) * (d / 4 / kColGroup);
+  const int groups = d / 4 / (d == 64 ? col_group<64>() : col_group<128>());
+  const long long blocks = (long long)grid * (part_rows / 128) * groups;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   if (d == 64) return launch_merge_d<64>(mp, bf16, (int)blocks, st);
   if (d == 128) return launch_merge_d<128>(mp, bf16, (int)blocks, st);
