@@ -181,34 +181,114 @@ def oss20b_chunk(layer: int, chunk: int, chunk_len: int = 512,
                       name=f"oss20b-L{layer}-c{chunk}")
 
 
+@dataclass
+class PrefillStack:
+    """The per-layer tensors of a chunked prefill, each kind stacked over the
+    layers: q [layers, seq, Hq, d], k and v [layers, seq, Hkv, d] (one KV
+    cache per layer, filled up to the current chunk).  Rows [c*L, (c+1)*L) of
+    every layer are then evenly spaced in memory, so one strided copy moves a
+    chunk of all layers."""
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    sinks: List[torch.Tensor]
+    windows: List[int]
+    chunk_len: int
+    scale: float
+
+    @property
+    def num_layers(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def num_chunks(self) -> int:
+        return int(self.q.shape[1]) // self.chunk_len
+
+    def chunk_meta(self, chunk: int, device=None) -> torch.Tensor:
+        """int32 [5] = (cu_seqlens_q[0:2], prefix_lens[0], kv_indptr[0:2]) of chunk."""
+        L = self.chunk_len
+        return torch.tensor([0, L, L * chunk, 0, L * (chunk + 1)], dtype=torch.int32,
+                            device=device if device is not None else self.q.device)
+
+    def call(self, chunk: int, layer: int, meta: Optional[torch.Tensor] = None) -> Batch:
+        """Chunk `chunk` of layer `layer`: query rows [c*L, (c+1)*L) over the
+        first (c+1)*L keys.  `meta` (from chunk_meta) holds the metadata; the
+        batch's metadata tensors are views of it."""
+        L = self.chunk_len
+        lo, hi = chunk * L, (chunk + 1) * L
+        m = meta if meta is not None else self.chunk_meta(chunk)
+        return Batch(self.q[layer, lo:hi], self.k[layer, :hi], self.v[layer, :hi],
+                     m[0:2], m[2:3], m[3:5], int(self.q.shape[2]), int(self.k.shape[2]),
+                     int(self.q.shape[3]), self.windows[layer], self.sinks[layer], False,
+                     self.scale, f"oss20b-L{layer}-c{chunk}",
+                     {"max_seqlen_q": L, "extend_lens": [L]})
+
+
+def oss20b_stack(num_layers: int = 24, seq: int = 16384, chunk_len: int = 512,
+                 seed: int = 3, device="cpu") -> PrefillStack:
+    """The tensors of a gpt-oss-20b-like prefill of `seq` tokens in chunks of
+    `chunk_len`: layers alternate full-causal (even) and window-128 (odd),
+    64/8 heads, d 64, bf16, per-head sinks; layer l draws from its own seed."""
+    layers = [make_batch([0], [seq], 64, 8, 64, "bf16", window=0 if layer % 2 == 0 else 128,
+                         sink_mode="head", seed=seed * 100003 + layer, device=device,
+                         name=f"oss20b-L{layer}")
+              for layer in range(num_layers)]
+    st = PrefillStack(torch.stack([t.q for t in layers]), torch.stack([t.k for t in layers]),
+                      torch.stack([t.v for t in layers]), [t.sinks for t in layers],
+                      [t.window for t in layers], chunk_len, layers[0].scale)
+    return st
+
+
 def oss20b_prefill(num_layers: int = 24, seq: int = 16384, chunk_len: int = 512,
                    seed: int = 3, device="cpu") -> List[List[Batch]]:
     """The calls of a gpt-oss-20b-like prefill of `seq` tokens in chunks of
-    `chunk_len`: calls[c][layer] for chunk c and layer, layers alternating
-    full-causal (even) and window-128 (odd).  Each layer has one KV cache of
-    `seq` tokens and one query tensor; chunk c is a view of query rows
-    [c*chunk_len, (c+1)*chunk_len) over the first (c+1)*chunk_len keys."""
-    n_chunks = seq // chunk_len
-    layers = []
-    for layer in range(num_layers):
-        full = make_batch([0], [seq], 64, 8, 64, "bf16", window=0 if layer % 2 == 0 else 128,
-                          sink_mode="head", seed=seed * 100003 + layer, device=device,
-                          name=f"oss20b-L{layer}")
-        layers.append(full)
+    `chunk_len`: calls[c][layer] for chunk c and layer (see oss20b_stack);
+    chunk c is a view of query rows [c*chunk_len, (c+1)*chunk_len) over the
+    first (c+1)*chunk_len keys of its layer."""
+    st = oss20b_stack(num_layers, seq, chunk_len, seed, device)
     calls = []
-    for c in range(n_chunks):
-        row = []
-        for layer, t in enumerate(layers):
-            lo, hi = c * chunk_len, (c + 1) * chunk_len
-            row.append(Batch(t.q[lo:hi], t.k[:hi], t.v[:hi],
-                             torch.tensor([0, chunk_len], dtype=torch.int32, device=device),
-                             torch.tensor([lo], dtype=torch.int32, device=device),
-                             torch.tensor([0, hi], dtype=torch.int32, device=device),
-                             64, 8, 64, t.window, t.sinks, False, t.scale,
-                             f"oss20b-L{layer}-c{c}", {"max_seqlen_q": chunk_len,
-                                                       "extend_lens": [chunk_len]}))
-        calls.append(row)
+    for c in range(st.num_chunks):
+        meta = st.chunk_meta(c)
+        calls.append([st.call(c, layer, meta) for layer in range(num_layers)])
     return calls
+
+
+def pack_custom_mask(keep_rows):
+    """Packs per-sequence boolean matrices keep_rows[b] [E_b, E_b] (row i,
+    extend key j') into the custom-mask layout: 32-bit words, row i of
+    sequence b at words mask_indptr[b] + i * W_b .. + W_b - 1 with
+    W_b = ceil(E_b / 32), key j' at bit j' % 32 of word j' / 32.  Returns
+    (words int32 tensor, mask_indptr int32 tensor [B+1])."""
+    import numpy as np
+    words, indptr = [], [0]
+    for m in keep_rows:
+        m = np.asarray(m, dtype=bool)
+        e = m.shape[0]
+        wb = (e + 31) // 32
+        padded = np.zeros((e, wb * 32), dtype=bool)
+        padded[:, :m.shape[1]] = m
+        packed = np.packbits(padded, axis=1, bitorder="little")  # bytes, key j' at bit j' % 8
+        words.append(np.ascontiguousarray(packed).view("<u4").reshape(-1))
+        indptr.append(indptr[-1] + e * wb)
+    flat = np.concatenate(words) if words else np.zeros(0, dtype=np.uint32)
+    return (torch.from_numpy(flat.astype(np.uint32).view(np.int32).copy()),
+            torch.tensor(indptr, dtype=torch.int32))
+
+
+def random_custom_mask(extend_lens, density=0.7, seed=0, diagonal=True):
+    """Seeded random keep matrices [E_b, E_b] per sequence (each entry kept
+    with probability `density`; the diagonal kept when `diagonal`), the way a
+    speculative-decoding draft tree hands its verify step an arbitrary
+    ancestor mask."""
+    import numpy as np
+    rng = np.random.default_rng(int(seed))
+    out = []
+    for e in extend_lens:
+        m = rng.random((e, e)) < density
+        if diagonal:
+            np.fill_diagonal(m, True)
+        out.append(m)
+    return out
 
 
 RAGGED_WINDOWS = [1, 15, 64, 127, 128, 129, 4096, 0]

@@ -56,6 +56,9 @@ def _bind(lib):
         ctypes.c_long, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_double, ctypes.c_int, dp, ctypes.c_int,
         ctypes.POINTER(ctypes.c_uint8), dp, dp]
+    lib.gqa_oracle_prefill_masked.restype = ctypes.c_int
+    lib.gqa_oracle_prefill_masked.argtypes = lib.gqa_oracle_prefill.argtypes + [
+        ctypes.POINTER(ctypes.c_uint32), i32p]
     lib.gqa_oracle_tile_census.restype = ctypes.c_long
     lib.gqa_oracle_tile_census.argtypes = [
         i32p, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -121,18 +124,30 @@ def _as_i32(x):
     return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
 
 
+def _as_u32(x):
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(x).astype(np.uint32, copy=False))
+
+
 def num_threads() -> int:
     return int(load().gqa_oracle_num_threads())
 
 
 def prefill(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, scale, window=0,
-            sinks=None, smooth_softmax=False, rows=None, lib=None, out=None, lse=None):
+            sinks=None, smooth_softmax=False, rows=None, lib=None, out=None, lse=None,
+            custom_mask=None, mask_indptr=None):
     """Run the oracle.  q [total_q,Hq,d]; k,v [total_kv,Hkv,d]; metadata as
     int arrays.  ``rows`` optionally lists the token rows to compute (the
     others come back as NaN, or untouched when ``out``/``lse`` are given:
     caller-owned contiguous float64 buffers of the result shapes, reused
-    across calls).  Returns (out float64 [total_q,Hq,d],
-    lse float64 [total_q,Hq])."""
+    across calls).  ``custom_mask`` (uint32 words) and ``mask_indptr``
+    (int32 [B+1]) add the custom-mask condition (see gqa_oracle.c).
+    Returns (out float64 [total_q,Hq,d], lse float64 [total_q,Hq])."""
     lib = lib or load()
     q64, k64, v64 = _as_f64(q), _as_f64(k), _as_f64(v)
     cu, pre, kvi = _as_i32(cu_seqlens_q), _as_i32(prefix_lens), _as_i32(kv_indptr)
@@ -151,7 +166,7 @@ def prefill(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, scale, window=0,
         sel = np.zeros(total_q, dtype=np.uint8)
         sel[np.asarray(rows, dtype=np.int64)] = 1
     s64 = None if sinks is None else _as_f64(sinks).reshape(hq)
-    rc = lib.gqa_oracle_prefill(
+    args = [
         _ptr(q64, ctypes.c_double), _ptr(k64, ctypes.c_double),
         _ptr(v64, ctypes.c_double), _ptr(cu, ctypes.c_int32),
         _ptr(pre, ctypes.c_int32), _ptr(kvi, ctypes.c_int32), num_seqs,
@@ -159,7 +174,14 @@ def prefill(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, scale, window=0,
         None if s64 is None else _ptr(s64, ctypes.c_double),
         1 if smooth_softmax else 0,
         None if sel is None else _ptr(sel, ctypes.c_uint8),
-        _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double))
+        _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double)]
+    if custom_mask is None:
+        rc = lib.gqa_oracle_prefill(*args)
+    else:
+        words = _as_u32(custom_mask)
+        mip = _as_i32(mask_indptr)
+        rc = lib.gqa_oracle_prefill_masked(*args, _ptr(words, ctypes.c_uint32),
+                                           _ptr(mip, ctypes.c_int32))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return out, lse

@@ -39,6 +39,17 @@
  *   4. a row with no kept key gets out = 0 and lse = -inf ([HIPEP] sink-fold
  *      commit: such a row is skipped and keeps a clamped denominator).
  *
+ *   Optional custom mask (gqa_oracle_prefill_masked): one more condition on
+ *   a key, ANDed with the causal and window conditions of step 2 ([SGL]
+ *   PR body: custom-mask and causal conjuncts can only empty a tile
+ *   further; the custom mask combined with a sliding window is the EAGLE
+ *   target-verify route of [SGL] commit 1).  The mask is a bitmap over each
+ *   sequence's extend keys: extend key P + j' is kept for extend row i only
+ *   if bit j' of row i is set; the prefix keys are not covered by it.
+ *   Layout: 32-bit words, row i of sequence b at words
+ *   mask_indptr[b] + i*W .. + W - 1 with W = ceil(E / 32), bit j' % 32 of
+ *   word j' / 32.
+ *
  * Precision: every input is the exact value of the caller's 16-bit number,
  * widened to double; all arithmetic is double (the pages' own references
  * accumulate in fp32; double is at least as exact).
@@ -58,6 +69,18 @@ static int oracle_keep(long pos, long j, int window)
     if (j > pos) return 0;                       /* causal */
     if (window > 0 && j < pos - window + 1) return 0; /* window lower bound */
     return 1;
+}
+
+/* Custom-mask condition (see above): 1 for a prefix key or without a mask,
+ * else bit (j - P) of row i of sequence b's bitmap. */
+static int oracle_custom_keep(const uint32_t* mask, const int32_t* mask_indptr, int b,
+                              long E, long P, long i, long j)
+{
+    if (mask == NULL || j < P) return 1;
+    const long jp = j - P;
+    const long W = (E + 31) / 32;
+    const uint32_t word = mask[(long)mask_indptr[b] + i * W + jp / 32];
+    return (int)((word >> (jp % 32)) & 1u);
 }
 
 /* Reports how many threads the oracle will use (for the CPU-baseline line). */
@@ -101,6 +124,14 @@ static int oracle_check_meta(const int32_t* cu, const int32_t* prefix,
  *   sinks [Hq] double or NULL; smooth nonzero selects the "+1" mode.
  * Returns 0, or -1 on inconsistent arguments.
  */
+int gqa_oracle_prefill_masked(const double* q, const double* k, const double* v,
+                              const int32_t* cu_seqlens_q, const int32_t* prefix_lens,
+                              const int32_t* kv_indptr, int num_seqs, long total_q,
+                              long total_kv, int Hq, int Hkv, int d, double scale,
+                              int window, const double* sinks, int smooth,
+                              const uint8_t* row_select, double* out, double* lse,
+                              const uint32_t* custom_mask, const int32_t* mask_indptr);
+
 int gqa_oracle_prefill(const double* q, const double* k, const double* v,
                        const int32_t* cu_seqlens_q, const int32_t* prefix_lens,
                        const int32_t* kv_indptr, int num_seqs, long total_q,
@@ -108,11 +139,37 @@ int gqa_oracle_prefill(const double* q, const double* k, const double* v,
                        int window, const double* sinks, int smooth,
                        const uint8_t* row_select, double* out, double* lse)
 {
+    return gqa_oracle_prefill_masked(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs,
+                                     total_q, total_kv, Hq, Hkv, d, scale, window, sinks,
+                                     smooth, row_select, out, lse, NULL, NULL);
+}
+
+/*
+ * gqa_oracle_prefill_masked -- gqa_oracle_prefill with the optional custom
+ * mask (custom_mask and mask_indptr both NULL: no mask).  mask_indptr
+ * [num_seqs+1] must step by E_b * ceil(E_b / 32) words per sequence.
+ */
+int gqa_oracle_prefill_masked(const double* q, const double* k, const double* v,
+                              const int32_t* cu_seqlens_q, const int32_t* prefix_lens,
+                              const int32_t* kv_indptr, int num_seqs, long total_q,
+                              long total_kv, int Hq, int Hkv, int d, double scale,
+                              int window, const double* sinks, int smooth,
+                              const uint8_t* row_select, double* out, double* lse,
+                              const uint32_t* custom_mask, const int32_t* mask_indptr)
+{
     if (Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return -1;
     if (sinks != NULL && smooth) return -1;
     if (oracle_check_meta(cu_seqlens_q, prefix_lens, kv_indptr, num_seqs,
                           total_q, total_kv) != 0)
         return -1;
+    if ((custom_mask == NULL) != (mask_indptr == NULL)) return -1;
+    if (mask_indptr != NULL) {
+        if (num_seqs > 0 && mask_indptr[0] < 0) return -1;
+        for (int b = 0; b < num_seqs; ++b) {
+            const long E = (long)cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+            if ((long)mask_indptr[b + 1] - mask_indptr[b] != E * ((E + 31) / 32)) return -1;
+        }
+    }
     const int G = Hq / Hkv;
     const long n_pairs = (long)num_seqs * Hq;
 
@@ -154,6 +211,7 @@ int gqa_oracle_prefill(const double* q, const double* k, const double* v,
                 double m = -INFINITY;
                 for (long j = 0; j < L; ++j) {
                     if (!oracle_keep(pos, j, window)) continue;
+                    if (!oracle_custom_keep(custom_mask, mask_indptr, b, E, P, i, j)) continue;
                     if (!any || s[j] > m) m = s[j];
                     any = 1;
                 }
@@ -168,6 +226,7 @@ int gqa_oracle_prefill(const double* q, const double* k, const double* v,
                 for (int t = 0; t < d; ++t) acc[t] = 0.0;
                 for (long j = 0; j < L; ++j) {
                     if (!oracle_keep(pos, j, window)) continue;
+                    if (!oracle_custom_keep(custom_mask, mask_indptr, b, E, P, i, j)) continue;
                     const double p = exp(s[j] - m);
                     z += p;
                     const double* vr = v + ((size_t)(base + j) * Hkv + g) * d;

@@ -28,6 +28,15 @@ MUTATIONS = {
                                "if (n0 <= pos && n1 > lo) {"),
     "census_masked_off_by_one": ("if (n0 < lo || n1 > pos) { ++masked; break; }",
                                  "if (n0 < lo || n1 >= pos) { ++masked; break; }"),
+    "custom_mask_ignored": ("if (mask == NULL || j < P) return 1;", "return 1;"),
+    "custom_mask_transposed": (
+        "const uint32_t word = mask[(long)mask_indptr[b] + i * W + jp / 32];\n"
+        "    return (int)((word >> (jp % 32)) & 1u);",
+        "const uint32_t word = mask[(long)mask_indptr[b] + jp * W + i / 32];\n"
+        "    return (int)((word >> (i % 32)) & 1u);"),
+    "custom_mask_bit_off_by_one": ("return (int)((word >> (jp % 32)) & 1u);",
+                                   "return (int)((word >> ((jp + 1) % 32)) & 1u);"),
+    "custom_mask_row_stride": ("const long W = (E + 31) / 32;", "const long W = E / 32;"),
     "census_window_ignored": ("long lo = (window > 0) ? pos - window + 1 : 0;",
                               "long lo = 0;"),
 }

@@ -260,12 +260,119 @@ def pin_sglang_tile_count_example(lib):
     assert before == g["tiles_before"]
 
 
+def _run_masked(lib, batch, keep_rows, window=None):
+    words, indptr = W.pack_custom_mask(keep_rows)
+    return oracle.prefill(batch.q, batch.k, batch.v, batch.cu_seqlens_q, batch.prefix_lens,
+                          batch.kv_indptr, batch.scale,
+                          batch.window if window is None else window, sinks=batch.sinks,
+                          smooth_softmax=batch.smooth, lib=lib, custom_mask=words,
+                          mask_indptr=indptr)
+
+
+def _masked_library_reference(batch, keep_rows):
+    """torch float64 softmax over scores with an explicit boolean keep matrix
+    per sequence: the tril/triu band of the causal/window mask, with its
+    extend columns ANDed with the custom keep matrix (the prefix columns
+    untouched); a sink is a dropped extra column."""
+    g = batch.hq // batch.hkv
+    q, k, v = (batch.q.to(torch.float64), batch.k.to(torch.float64),
+               batch.v.to(torch.float64))
+    out = torch.zeros_like(q)
+    lse = torch.zeros(q.shape[:2], dtype=torch.float64)
+    w = batch.window
+    for b, q0, q1, k0, k1, p in _seq_slices(batch):
+        e, L = q1 - q0, k1 - k0
+        ones = torch.ones(e, L, dtype=torch.bool)
+        keep = torch.tril(ones, diagonal=p)
+        if w > 0:
+            keep = keep & torch.triu(ones, diagonal=p - w + 1)
+        keep[:, p:] &= torch.from_numpy(np.asarray(keep_rows[b], dtype=bool))
+        for h in range(batch.hq):
+            s = batch.scale * q[q0:q1, h] @ k[k0:k1, h // g].T
+            s = s.masked_fill(~keep, float("-inf"))
+            if batch.sinks is not None or batch.smooth:
+                x = 0.0 if batch.smooth else float(batch.sinks[h])
+                s = torch.cat([s, torch.full((e, 1), x, dtype=torch.float64)], 1)
+            pr = torch.softmax(s, dim=1)[:, :L]
+            out[q0:q1, h] = pr @ v[k0:k1, h // g]
+            lse[q0:q1, h] = torch.logsumexp(s, dim=1)
+    return out.numpy(), lse.numpy()
+
+
+def pin_custom_mask_is_library_masked_softmax(lib):
+    """A random custom mask ANDed into the causal/window mask, against the
+    library softmax over an explicit keep matrix (packed by numpy, so the
+    oracle's bit layout is checked too); widths across the 32-bit words."""
+    for w, mode in ((0, "head"), (9, "none"), (25, "smooth")):
+        b = W.make_batch([0, 37, 5], [23, 45, 70], 4, 2, 16, "bf16", window=w,
+                         sink_mode=mode, seed=91 + w)
+        keep = W.random_custom_mask(b.extend_lens, density=0.6, seed=w)
+        out, lse = _run_masked(lib, b, keep)
+        ref, ref_lse = _masked_library_reference(b, keep)
+        np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse, ref_lse, rtol=0, atol=1e-12)
+
+
+def pin_custom_mask_full_or_causal_is_no_mask(lib):
+    """All-ones and lower-triangular custom masks change nothing (causality
+    already removes every key above the diagonal): bit-identical."""
+    b = _small_ragged(11, "head", seed=92)
+    ref, ref_lse = _run(lib, b)
+    for keep in ([np.ones((e, e), bool) for e in b.extend_lens],
+                 [np.tril(np.ones((e, e), bool)) for e in b.extend_lens]):
+        out, lse = _run_masked(lib, b, keep)
+        assert np.array_equal(out, ref) and np.array_equal(lse, ref_lse)
+
+
+def pin_custom_mask_diagonal_is_window_one(lib):
+    """Without a prefix, a custom mask keeping only the diagonal leaves each
+    row its own key: the window = 1 result, bit for bit."""
+    b = W.make_batch([0, 0], [33, 20], 4, 2, 16, "f16", window=0, sink_mode="head", seed=93)
+    out, lse = _run_masked(lib, b, [np.eye(e, dtype=bool) for e in b.extend_lens])
+    ref, ref_lse = _run(lib, b, window=1)
+    assert np.array_equal(out, ref) and np.array_equal(lse, ref_lse)
+
+
+def pin_custom_mask_counting_probe(lib):
+    """q = 0 and v[j] = (1, j, j^2): each row's output recovers the exact set
+    of keys it kept -- every prefix key inside the window, plus the extend
+    keys whose bit is set, at or below the row, inside the window."""
+    for w in (0, 7, 40):
+        p, e = 13, 50
+        b = W.make_batch([p], [e], 2, 1, 8, "f16", window=w, sink_mode="head", seed=94)
+        b.q.zero_()
+        L = p + e
+        j = torch.arange(L, dtype=torch.float64)
+        b.v.zero_()
+        b.v[:, 0, 0] = 1.0
+        b.v[:, 0, 1] = j.to(b.v.dtype)
+        b.v[:, 0, 2] = (j * j).to(b.v.dtype)
+        keep = W.random_custom_mask([e], density=0.5, seed=95 + w, diagonal=False)
+        out, lse = _run_masked(lib, b, keep)
+        for h in range(2):
+            es = np.exp(float(b.sinks[h]))
+            for i in range(e):
+                pos = p + i
+                lo = 0 if w <= 0 else max(0, pos - w + 1)
+                keys = [jj for jj in range(lo, pos + 1) if jj < p or keep[0][i, jj - p]]
+                n = len(keys)
+                if n == 0:
+                    assert np.all(out[i, h] == 0) and lse[i, h] == -np.inf
+                    continue
+                den = n + es
+                vs = b.v[keys, 0, :3].double().numpy()  # j^2 as stored (fp16-rounded past 2048)
+                np.testing.assert_allclose(out[i, h, :3], vs.sum(axis=0) / den, rtol=1e-12)
+                np.testing.assert_allclose(lse[i, h], np.log(den), rtol=1e-12)
+
+
 PINS = [pin_plain_causal_is_library_softmax, pin_sinks_are_a_dropped_softmax_column,
         pin_window_is_library_band, pin_window_one_closed_form,
         pin_wide_window_equals_no_window, pin_smooth_equals_zero_sinks,
         pin_counting_probe, pin_chunked_equals_one_shot,
         pin_window_bounded_layout_equals_full, pin_row_selection_is_exact,
-        pin_tile_census_brute_force, pin_sglang_tile_count_example]
+        pin_tile_census_brute_force, pin_sglang_tile_count_example,
+        pin_custom_mask_is_library_masked_softmax, pin_custom_mask_full_or_causal_is_no_mask,
+        pin_custom_mask_diagonal_is_window_one, pin_custom_mask_counting_probe]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
