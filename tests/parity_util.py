@@ -8,14 +8,18 @@ from gqa_flash_attention_prefill_gb300 import workloads as W
 
 # Tolerances for 16-bit inputs with fp32 accumulation: relL2 <= 1e-3 and
 # max_abs <= 2e-2, lse within 1e-3.  For bf16 outputs the relL2 bound adds the
-# quantisation floor of the dtype itself: rounding the EXACT result to bf16
-# already costs qf = relL2(bf16(ref), ref) ~ 1.6e-3 on these inputs, and the
-# probabilities fed to the P.V tensor-core product are bf16 too (A and B of one
-# MMA share a type), which adds a term of the same size.  So bf16 uses
-# 1e-3 + 2 * qf, with qf measured on the case's own oracle output.
+# quantisation floor of the dtype itself, once: rounding the EXACT result to
+# bf16 already costs qf = relL2(bf16(ref), ref) ~ 1.6e-3 on N(0,1) inputs, so
+# no bf16 output can meet 1e-3.  bf16 uses 1e-3 + qf, with qf measured on the
+# case's own oracle output.
 REL_L2 = 1e-3
 MAX_ABS = 2e-2
 LSE_ABS = 1e-3
+
+# Every comparison made in this process: (label, dtype, relL2, bound,
+# max_abs, lse error).  tests/conftest.py prints a summary at the end of the
+# run, so each bf16 case's margin is visible in the log.
+RESULTS = []
 
 
 def quant_floor(ref, dtype):
@@ -90,7 +94,8 @@ def compare(out, lse, ref, ref_lse, rows=None, label=""):
     lerr = float(np.abs(gl - ref_lse).max()) if gl.size else 0.0
     tol = REL_L2
     if dtype == torch.bfloat16:
-        tol = REL_L2 + 2.0 * quant_floor(ref, torch.bfloat16)
+        tol = REL_L2 + quant_floor(ref, torch.bfloat16)
+    RESULTS.append((label, "bf16" if dtype == torch.bfloat16 else "f16", rel, tol, mx, lerr))
     assert rel <= tol and mx <= MAX_ABS, \
         f"{label}: relL2={rel:.3e} (tol {tol:.3e}) max_abs={mx:.3e}"
     assert lerr <= LSE_ABS, f"{label}: lse max_abs={lerr:.3e}"
