@@ -1,18 +1,24 @@
 """Benchmark of the fused GQA flash-attention prefill on one GB300.
 
-Workload (one "step"): a gpt-oss layer pair in pure prefill -- batch 1, 4096
-tokens, Hq=64 / Hkv=8, d=64, bf16 Q/K/V ~ N(0,1) (synthetic: no model
-weights), per-head sinks ~ N(0,1), one full-causal layer and one window-128
-layer.  Both layers' inputs are resident in HBM before timing starts.
+Headline workload (one "step"): a gpt-oss-20b-like prefill of 16,384 tokens
+processed as 32 chunks of 512 over a growing cached prefix, through 24 layers
+alternating full-causal and window-128 attention -- 768 calls, chunk-major
+(the order a chunked prefill runs them).  Hq=64 / Hkv=8, d=64, bf16 Q/K/V
+~ N(0,1) (synthetic: no model weights), per-head sinks ~ N(0,1).  All
+inputs are resident in HBM before timing starts; they are far larger than
+L2 (3.8 GB read per step), and a 256 MiB buffer is also written between
+steps, outside the timed events.
 
 Metric: useful attention TFLOP/s = 4 * d * Hq * (unmasked query-key pairs) /
-time, counting only pairs the mask keeps; also prefill tokens/s and the
-fraction of the measured dense bf16 tensor peak.
+time, counting only pairs the mask keeps; also prefill tokens/s (attention
+only) and the fraction of the measured dense bf16 tensor peak.
 
-Between timed steps a 256 MiB buffer is written to flush the 126 MB L2; each
-step is timed alone with CUDA events on the launching stream, so the flush is
-outside the measured time.  `--impl reference` times the CPU oracle instead
-(on a bounded sample of rows of the same workload).
+The line also carries the gpt-oss layer pair (4096 tokens, one full-causal
+and one window-128 layer) as a sub-object, the per-kernel rooflines, an
+end-to-end figure through the C ABI from pinned host buffers, and the CPU
+oracle timed on a bounded sample.  `--impl reference` times the CPU oracle
+instead (a bounded sample of rows of the same workload); `--workload`
+selects the supplementary configurations.
 """
 from __future__ import annotations
 
@@ -31,7 +37,12 @@ sys.path.insert(0, ROOT)
 
 METRIC = "useful attention TFLOP/s & prefill tok/s at 1 GB300; % of bf16 tensor peak"
 UNIT = "TFLOP/s"
-WORKLOAD = "gpt-oss layer pair, pure prefill: B=1, seq 4096, Hq=64, Hkv=8, d=64, bf16, full-causal + window-128, per-head sinks"
+WORKLOAD = ("gpt-oss-20b-like 16k prefill: 24 layers alternating full-causal and window-128 "
+            "(12 each), Hq=64, Hkv=8, d=64, bf16, 16384 tokens as 32 chunks of 512 over a "
+            "growing prefix, per-head sinks (768 calls per step)")
+PAIR_WORKLOAD = ("gpt-oss layer pair, pure prefill: B=1, seq 4096, Hq=64, Hkv=8, d=64, bf16, "
+                 "full-causal + window-128, per-head sinks")
+SEQ, CHUNK, LAYERS = 16384, 512, 24
 
 
 def useful_pairs(prefix_lens, extend_lens, window):
@@ -72,9 +83,10 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per launch of the full-causal kernel from the committed ncu
-    summary, or None when the kernel sources changed since it was taken."""
+def recorded_traffic(key):
+    """DRAM bytes per launch recorded under `key` in the committed ncu summary
+    (profiles/traffic.json), or None when the kernel sources changed since
+    the counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -82,7 +94,7 @@ def recorded_traffic():
         rec = json.load(f)
     if rec.get("kernel_source_hash") != kernel_source_hash():
         return None
-    return rec.get("full_layer_dram_bytes_per_launch")
+    return rec.get(key)
 
 
 class ClockSampler:
@@ -179,7 +191,8 @@ def dist_barrier(world):
         dist.barrier()
 
 
-def run_ours(args, rank, world):
+def run_layer_pair(args, rank, world):
+    """The gpt-oss layer pair as the workload (`--workload layer_pair`)."""
     import torch
     import gqa_flash_attention_prefill_gb300 as pkg
     from gqa_flash_attention_prefill_gb300 import workloads as W
@@ -229,14 +242,14 @@ def run_ours(args, rank, world):
     dist_barrier(world)
     t_full = [e[0].elapsed_time(e[1]) for e in ev]
     t_win = [e[1].elapsed_time(e[2]) for e in ev]
-    ms_step = statistics.mean(a + b for a, b in zip(t_full, t_win))
+    ms_step = statistics.median(a + b for a, b in zip(t_full, t_win))
     ms_step = dist_max(ms_step, world)
     if pkg.get_device_status() != 0:
         raise RuntimeError("device status word raised during the timed region")
 
     peaks = load_peaks()
     value = world * sum(flops) / (ms_step * 1e-3) / 1e12
-    full_ms = statistics.mean(t_full)
+    full_ms = statistics.median(t_full)
     achieved = flops[0] / (full_ms * 1e-3) / 1e12
 
     # The same launches without the L2 flush (the layer pair's 75 MB of
@@ -250,7 +263,7 @@ def run_ours(args, rank, world):
         pkg.prefill(layers[1], out=outs[1], lse=lses[1], stream=stream)
         ev_w[i][1].record(stream)
     torch.cuda.synchronize()
-    warm_ms = dist_max(statistics.mean(e[0].elapsed_time(e[1]) for e in ev_w), world)
+    warm_ms = dist_max(statistics.median(e[0].elapsed_time(e[1]) for e in ev_w), world)
 
     # End to end through the C ABI from pinned host buffers: per step, copy
     # this step's inputs host->device, run both layers, read the outputs back.
@@ -317,19 +330,19 @@ def run_ours(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) Q/K/V and sinks; no model weights)",
-        "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": args.seq,
+        "config": {"workload": PAIR_WORKLOAD, "global_batch": world, "seq_len": args.seq,
                    "layers": ["full-causal", "window-128"], "l2": "flushed between steps (256 MiB write)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "tokens_per_s": round(world * tokens / 2 / (ms_step * 1e-3), 1),
         "pct_of_bf16_peak": round(100.0 * value / (world * peaks["bf16_tflops"]), 2),
         "per_layer_ms": {"full_causal": round(full_ms, 5),
-                         "window_128": round(statistics.mean(t_win), 5)},
+                         "window_128": round(statistics.median(t_win), 5)},
         "per_layer_tflops": {"full_causal": round(achieved, 2),
-                             "window_128": round(flops[1] / (statistics.mean(t_win) * 1e-3) / 1e12, 2)},
+                             "window_128": round(flops[1] / (statistics.median(t_win) * 1e-3) / 1e12, 2)},
         "roofline": {"bound": "tensor", "kernel": "prefill_kernel<64,128,...,full-causal>",
                      "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                     "traffic": recorded_traffic(), "peak_source": peaks["source"] + " burst bf16"},
+                     "traffic": recorded_traffic("full_layer_dram_bytes_per_launch"), "peak_source": peaks["source"] + " burst bf16"},
         "e2e": {"value": round(world * sum(flops) / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
@@ -342,6 +355,381 @@ def run_ours(args, rank, world):
                     "unit": UNIT, "note": "no L2 flush between steps; not the headline"},
     }
     return line
+
+
+# ----------------------------------------------------------------- headline: 16k prefill
+
+def chunk_pairs(prefix, extend, window):
+    """Unmasked (query, key) pairs per head of one call with a single
+    sequence: rows i < extend see min(prefix + i + 1, window) keys (all
+    prefix + i + 1 without a window)."""
+    n = sum(prefix + i + 1 for i in range(extend)) if window <= 0 else \
+        sum(min(prefix + i + 1, window) for i in range(extend))
+    return n
+
+
+def window_call_bytes(prefix, extend, hq, hkv, d, window, elt=2):
+    """Minimum HBM bytes of one windowed call: Q read and O written once, lse
+    written, and of K and V only the rows some query's window reaches
+    (min(prefix, window - 1) prefix rows plus the chunk's own)."""
+    keys = min(prefix, window - 1) + extend
+    return extend * hq * d * elt * 2 + extend * hq * 4 + keys * hkv * d * elt * 2
+
+
+class Cudart:
+    """cudaMemcpy2DAsync from the CUDA runtime already loaded by torch: one
+    strided copy moves a chunk's rows of every layer (a layer-stacked device
+    tensor and a chunk-major host buffer)."""
+
+    H2D, D2H = 1, 2
+
+    def __init__(self):
+        import ctypes
+        lib = None
+        for name in ("libcudart.so.13", "libcudart.so.12", "/usr/local/cuda/lib64/libcudart.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if lib is None:
+            raise RuntimeError("CUDA runtime library not found")
+        c = ctypes
+        lib.cudaMemcpy2DAsync.argtypes = [c.c_void_p, c.c_size_t, c.c_void_p, c.c_size_t,
+                                          c.c_size_t, c.c_size_t, c.c_int, c.c_void_p]
+        lib.cudaMemcpy2DAsync.restype = c.c_int
+        self.lib = lib
+
+    def copy2d(self, dst, dpitch, src, spitch, width, height, kind, stream):
+        rc = self.lib.cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, height, kind,
+                                        stream.cuda_stream)
+        if rc != 0:
+            raise RuntimeError(f"cudaMemcpy2DAsync failed: {rc}")
+
+
+def oss20b_setup(device="cuda", num_layers=LAYERS, seq=SEQ, chunk=CHUNK):
+    """The 16k prefill's tensors (layer-stacked), its 768 calls in chunk-major
+    order, and per call its kind, useful flops and minimum bytes."""
+    from gqa_flash_attention_prefill_gb300 import workloads as W
+    st = W.oss20b_stack(num_layers=num_layers, seq=seq, chunk_len=chunk, seed=3, device=device)
+    metas = [st.chunk_meta(c, device) for c in range(st.num_chunks)]
+    calls = []
+    for c in range(st.num_chunks):
+        for layer in range(st.num_layers):
+            b = st.call(c, layer, metas[c])
+            p = c * chunk
+            fl = 4.0 * b.d * b.hq * chunk_pairs(p, chunk, b.window)
+            nb = window_call_bytes(p, chunk, b.hq, b.hkv, b.d, b.window) if b.window > 0 else 0
+            calls.append({"chunk": c, "layer": layer, "batch": b, "flops": fl, "bytes": nb,
+                          "kind": "window_128" if b.window > 0 else "full_causal"})
+    return st, metas, calls
+
+
+def run_oss20b(args, rank, world):
+    """Headline: the 16k chunked prefill, 768 calls per step."""
+    import torch
+    import gqa_flash_attention_prefill_gb300 as pkg
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    pkg.load()
+    st, metas, calls = oss20b_setup()
+    out = torch.empty_like(st.q)
+    lse = torch.empty(st.q.shape[:3], dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    L = CHUNK
+    for cl in calls:
+        c, layer = cl["chunk"], cl["layer"]
+        cl["run"] = pkg.prepare(cl["batch"], out=out[layer, c * L:(c + 1) * L],
+                                lse=lse[layer, c * L:(c + 1) * L], stream=stream)
+    flops = sum(cl["flops"] for cl in calls)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+
+    def step():
+        for cl in calls:
+            cl["run"]()
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if pkg.get_device_status() != 0:
+        raise RuntimeError("device status word raised during warm-up")
+
+    # Timed region: K steps, each bracketed by events on the launching stream;
+    # the L2 flush sits between steps, outside the events.
+    steps = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        for i in range(steps):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall1 = time.perf_counter()
+        clk.mark(t_wall0, t_wall1)
+    dist_barrier(world)
+    t_steps = [e[0].elapsed_time(e[1]) for e in ev]
+    ms_step = dist_max(statistics.median(t_steps), world)
+    ms_mean = dist_max(statistics.mean(t_steps), world)
+    if pkg.get_device_status() != 0:
+        raise RuntimeError("device status word raised during the timed region")
+
+    # Per-kernel durations: the same steps again with an event between every
+    # two launches (on the launching stream), so each call's duration is known.
+    # The events keep each kernel from overlapping its neighbour, so these are
+    # the kernels' isolated times; the headline above has no such events.
+    n_b = max(1, min(steps, 10))
+    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+           for _ in range(n_b)]
+    for i in range(n_b):
+        flush.fill_(float(i))
+        evb[i][0].record(stream)
+        for j, cl in enumerate(calls):
+            cl["run"]()
+            evb[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    kind_ms = {"full_causal": 0.0, "window_128": 0.0}
+    for i in range(n_b):
+        for j, cl in enumerate(calls):
+            kind_ms[cl["kind"]] += evb[i][j].elapsed_time(evb[i][j + 1]) / n_b
+    kind_ms = {k: dist_max(v, world) for k, v in kind_ms.items()}
+    # isolated time per chunk and kind, averaged over the layers and steps
+    chunk_ms = {"full_causal": [0.0] * st.num_chunks, "window_128": [0.0] * st.num_chunks}
+    for i in range(n_b):
+        for j, cl in enumerate(calls):
+            chunk_ms[cl["kind"]][cl["chunk"]] += (evb[i][j].elapsed_time(evb[i][j + 1])
+                                                  / n_b / (st.num_layers // 2))
+    kind_flops = {k: sum(cl["flops"] for cl in calls if cl["kind"] == k) for k in kind_ms}
+    win_bytes = sum(cl["bytes"] for cl in calls if cl["kind"] == "window_128")
+    n_kind = {k: sum(1 for cl in calls if cl["kind"] == k) for k in kind_ms}
+    if pkg.get_device_status() != 0:
+        raise RuntimeError("device status word raised during the per-kernel pass")
+
+    peaks = load_peaks()
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    full_tf = kind_flops["full_causal"] / (kind_ms["full_causal"] * 1e-3) / 1e12
+    win_gbs = win_bytes / (kind_ms["window_128"] * 1e-3) / 1e9
+    e2e = oss20b_e2e(args, st, metas, calls, out, lse, stream, world, flops)
+    del flush
+    pair = layer_pair_summary(args, world, peaks)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) Q/K/V and sinks; no model weights)",
+        "config": bench_config(world),
+        "ms_per_step_mean": round(ms_mean, 4),
+        "tokens_per_s": round(world * SEQ / (ms_step * 1e-3), 1),
+        "pct_of_bf16_peak": round(100.0 * value / (world * peaks["bf16_tflops"]), 2),
+        "pct_of_bf16_peak_sustained": round(100.0 * value / (world * peaks["bf16_tflops_sustained"]), 2),
+        "roofline": {"bound": "tensor",
+                     "kernel": "prefill_kernel<64,128,...> full-causal calls (384 per step)",
+                     "achieved": round(full_tf, 2), "peak": peaks["bf16_tflops_sustained"],
+                     "unit": "TFLOP/s", "frac": round(full_tf / peaks["bf16_tflops_sustained"], 4),
+                     "frac_of_burst": round(full_tf / peaks["bf16_tflops"], 4),
+                     "traffic": recorded_traffic("oss20b_full_dram_bytes_per_launch"),
+                     "peak_source": peaks["source"] + " sustained bf16 (kernel timed inside a "
+                                                      "seconds-long loop)",
+                     "work": "useful flops (4 d Hq per unmasked pair) of the full-causal calls / "
+                             "their summed isolated durations"},
+        "roofline_window": {"bound": "hbm",
+                            "kernel": "prefill_kernel<64,64,...> window-128 calls (384 per step)",
+                            "achieved": round(win_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": round(win_gbs / peaks["hbm_gbs"], 4),
+                            "traffic": recorded_traffic("oss20b_window_dram_bytes_per_launch"),
+                            "algorithmic_bytes_per_launch": round(win_bytes / n_kind["window_128"]),
+                            "work": "Q read, O and lse written, K and V rows inside some "
+                                    "query's window read once"},
+        "per_kind": {k: {"calls": n_kind[k], "ms_per_step": round(kind_ms[k], 4),
+                         "useful_tflops": round(kind_flops[k] / (kind_ms[k] * 1e-3) / 1e12, 2)}
+                     for k in kind_ms},
+        "per_chunk_us": {k: [round(1e3 * x, 1) for x in v] for k, v in chunk_ms.items()},
+        "layer_pair": pair,
+        "e2e": e2e,
+        "gpu_launches": len(calls) * steps,
+        "clocks": clk.summary(),
+        "timed_wall_s": round(t_wall1 - t_wall0, 3),
+    }
+    return line
+
+
+def bench_config(world):
+    return {"workload": WORKLOAD, "global_batch": world, "seq_len": SEQ, "chunk_len": CHUNK,
+            "layers": LAYERS, "calls_per_step": LAYERS * (SEQ // CHUNK),
+            "l2": "inputs larger than L2 (3.8 GB read per step); 256 MiB written between steps",
+            "parallelism": "replicas (one per GPU)" if world > 1 else "single GPU",
+            "entry": "gqa_flash_prefill"}
+
+
+def oss20b_e2e(args, st, metas, calls, out, lse, stream, world, flops):
+    """The 16k prefill end to end through the C ABI from pinned host memory:
+    every step uploads each chunk's Q rows, its new K and V rows and its
+    metadata for all 24 layers, runs the chunk's 24 calls, and downloads the
+    chunk's output and lse rows.  Copies run on their own streams, one
+    strided copy per tensor and chunk, so uploads and downloads overlap the
+    kernels.  Consecutive steps alternate between two sets of device buffers
+    (as a server alternates between requests), so a step's uploads need not
+    wait for the previous step's last kernel, which still reads the K/V rows
+    they would overwrite."""
+    import torch
+    import gqa_flash_attention_prefill_gb300 as pkg
+    from gqa_flash_attention_prefill_gb300 import workloads as W
+    cr = Cudart()
+    n_l, n_c, L = st.num_layers, st.num_chunks, st.chunk_len
+    hq, hkv, d = st.q.shape[2], st.k.shape[2], st.q.shape[3]
+    # Chunk-major pinned host buffers: [chunk][layer][row][head][dim].
+    hq_ = torch.empty((n_c, n_l, L, hq, d), dtype=st.q.dtype, pin_memory=True)
+    hk_ = torch.empty((n_c, n_l, L, hkv, d), dtype=st.k.dtype, pin_memory=True)
+    hv_ = torch.empty((n_c, n_l, L, hkv, d), dtype=st.v.dtype, pin_memory=True)
+    hm_ = torch.stack([m.cpu() for m in metas]).pin_memory()
+    ho_ = torch.empty((n_c, n_l, L, hq, d), dtype=out.dtype, pin_memory=True)
+    hl_ = torch.empty((n_c, n_l, L, hq), dtype=torch.float32, pin_memory=True)
+    for c in range(n_c):
+        hq_[c].copy_(st.q[:, c * L:(c + 1) * L])
+        hk_[c].copy_(st.k[:, c * L:(c + 1) * L])
+        hv_[c].copy_(st.v[:, c * L:(c + 1) * L])
+    # Two device sets: the resident tensors and a second set of the same shapes.
+    st2 = W.PrefillStack(torch.empty_like(st.q), torch.empty_like(st.k), torch.empty_like(st.v),
+                         st.sinks, st.windows, st.chunk_len, st.scale)
+    metas2 = [torch.empty_like(m) for m in metas]
+    out2, lse2 = torch.empty_like(out), torch.empty_like(lse)
+    sets = []
+    for s_, m_, o_, l_ in ((st, metas, out, lse), (st2, metas2, out2, lse2)):
+        runs = [[pkg.prepare(s_.call(c, layer, m_[c]), out=o_[layer, c * L:(c + 1) * L],
+                             lse=l_[layer, c * L:(c + 1) * L], stream=stream)
+                 for layer in range(n_l)] for c in range(n_c)]
+        sets.append({"st": s_, "metas": m_, "out": o_, "lse": l_, "runs": runs,
+                     "in_ready": [torch.cuda.Event() for _ in range(n_c)],
+                     "done": [torch.cuda.Event() for _ in range(n_c)],
+                     "out_free": [torch.cuda.Event() for _ in range(n_c)],
+                     "step_done": torch.cuda.Event()})
+    for S in sets:
+        for e in S["out_free"] + [S["step_done"]]:
+            e.record(stream)
+    elt = st.q.element_size()
+    q_row, kv_row, o_row, l_row = hq * d * elt, hkv * d * elt, hq * d * out.element_size(), hq * 4
+    seq = st.q.shape[1]
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def up(dev_t, host_t, c, row_bytes):
+        # rows [c L, (c+1) L) of every layer: n_l blocks of L rows, one layer apart
+        cr.copy2d(dev_t.data_ptr() + c * L * row_bytes, seq * row_bytes, host_t[c].data_ptr(),
+                  L * row_bytes, L * row_bytes, n_l, Cudart.H2D, h2d_s)
+
+    def down(host_t, dev_t, c, row_bytes):
+        cr.copy2d(host_t[c].data_ptr(), L * row_bytes, dev_t.data_ptr() + c * L * row_bytes,
+                  seq * row_bytes, L * row_bytes, n_l, Cudart.D2H, d2h_s)
+
+    def e2e_step(S):
+        # This set's K/V rows were last read by its previous step's last kernel.
+        h2d_s.wait_event(S["step_done"])
+        s_ = S["st"]
+        for c in range(n_c):
+            up(s_.q, hq_, c, q_row)
+            up(s_.k, hk_, c, kv_row)
+            up(s_.v, hv_, c, kv_row)
+            with torch.cuda.stream(h2d_s):
+                S["metas"][c].copy_(hm_[c], non_blocking=True)
+            S["in_ready"][c].record(h2d_s)
+        for c in range(n_c):
+            stream.wait_event(S["in_ready"][c])
+            stream.wait_event(S["out_free"][c])
+            for r in S["runs"][c]:
+                r()
+            S["done"][c].record(stream)
+            d2h_s.wait_event(S["done"][c])
+            down(ho_, S["out"], c, o_row)
+            down(hl_, S["lse"], c, l_row)
+            S["out_free"][c].record(d2h_s)
+        S["step_done"].record(stream)
+
+    n_e = max(4, min(args.steps, 10))
+    for i in range(2):
+        e2e_step(sets[i % 2])
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    h2d_s.wait_event(e0)
+    d2h_s.wait_event(e0)
+    for i in range(n_e):
+        e2e_step(sets[i % 2])
+    for S in sets:
+        for e in S["out_free"]:
+            stream.wait_event(e)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = dist_max(e0.elapsed_time(e1) / n_e, world)
+    # the outputs of the last step match the device-resident run's
+    last = sets[(n_e - 1) % 2]
+    ok = bool(torch.equal(last["out"], out)) if last["out"] is not out else True
+    h2d = n_c * (n_l * L * (q_row + 2 * kv_row) + hm_[0].numel() * 4)
+    d2h = n_c * n_l * L * (o_row + l_row)
+    del st2, out2, lse2, sets
+    return {"value": round(world * flops / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
+            "ms_per_step": round(ms, 4), "steps": n_e, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "outputs_match_resident_run": ok,
+            "pipeline": "per chunk: strided uploads of Q, new K/V rows and metadata (all 24 "
+                        "layers), 24 calls, strided downloads of out and lse; copy-in, compute "
+                        "and copy-out streams; steps alternate between two device buffer sets"}
+
+
+def layer_pair_summary(args, world, peaks):
+    """The gpt-oss layer pair (4096 tokens), each layer timed alone with
+    events, L2 flushed before every step: per-layer time and the two
+    rooflines (full-causal: tensor, burst peak; window-128: HBM)."""
+    import torch
+    import gqa_flash_attention_prefill_gb300 as pkg
+    from gqa_flash_attention_prefill_gb300 import workloads as W
+    layers = [b.to("cuda") for b in W.layer_pair(seq=4096, seed=1)]
+    stream = torch.cuda.current_stream()
+    outs = [torch.empty_like(b.q) for b in layers]
+    lses = [torch.empty(b.q.shape[:2], dtype=torch.float32, device="cuda") for b in layers]
+    runs = [pkg.prepare(b, out=o, lse=l, stream=stream) for b, o, l in zip(layers, outs, lses)]
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    n = max(20, min(10 * args.steps, 200))
+    for _ in range(5):
+        flush.fill_(1.0)
+        for r in runs:
+            r()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    for i in range(n):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        runs[0]()
+        ev[i][1].record(stream)
+        runs[1]()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    if pkg.get_device_status() != 0:
+        raise RuntimeError("device status word raised in the layer pair")
+    t_full = dist_max(statistics.median(e[0].elapsed_time(e[1]) for e in ev), world)
+    t_win = dist_max(statistics.median(e[1].elapsed_time(e[2]) for e in ev), world)
+    fl = [4.0 * b.d * b.hq * chunk_pairs(0, b.total_q, b.window) for b in layers]
+    wb = window_call_bytes(0, layers[1].total_q, 64, 8, 64, 128)
+    full_tf = fl[0] / (t_full * 1e-3) / 1e12
+    return {"workload": PAIR_WORKLOAD, "steps": n,
+            "ms_per_step": round(t_full + t_win, 5),
+            "value": round(world * sum(fl) / ((t_full + t_win) * 1e-3) / 1e12, 2),
+            "per_layer_ms": {"full_causal": round(t_full, 5), "window_128": round(t_win, 5)},
+            "full_causal": {"bound": "tensor", "achieved": round(full_tf, 2),
+                            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                            "frac": round(full_tf / peaks["bf16_tflops"], 4),
+                            "traffic": recorded_traffic("full_layer_dram_bytes_per_launch"),
+                            "peak_source": peaks["source"] + " burst bf16 (one launch timed alone)"},
+            "window_128": {"bound": "hbm", "achieved": round(wb / (t_win * 1e-3) / 1e9, 1),
+                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": round(wb / (t_win * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                           "algorithmic_bytes": wb,
+                           "useful_tflops": round(fl[1] / (t_win * 1e-3) / 1e12, 2)},
+            "l2": "flushed before every step (256 MiB write)"}
 
 
 def run_ragged_grid(args, rank, world):
@@ -432,12 +820,6 @@ def run_workload(args, rank, world):
         desc = (f"chunked prefill over cached prefix: B=8, prefix 8192 + extend 8192, 64/8, d 64, "
                 f"bf16, window 128, sinks, {args.layout} KV layout")
         tokens = 8 * 8192
-    elif args.workload == "oss20b_16k":
-        grid = W.oss20b_prefill(num_layers=24, seq=16384, chunk_len=512, seed=3, device=dev)
-        calls = [c for row in grid for c in row]  # chunk-major: the prefill's order
-        desc = ("gpt-oss-20b-like 16k prefill: 24 layers (12 full, 12 window-128), 64/8, d 64, "
-                "bf16, 32 chunks of 512 over a growing prefix, sinks (768 calls per step)")
-        tokens = 16384
     elif args.workload == "ragged":
         b = W.ragged(hq=64, hkv=8, d=64, dtype="bf16", window=128, sink_mode="head", seed=4)
         calls = [b.to(dev)]
@@ -527,7 +909,7 @@ def run_workload(args, rank, world):
         torch.cuda.synchronize()
         clk.mark(t0, time.perf_counter())
     dist_barrier(world)
-    ms_step = dist_max(statistics.mean(e[0].elapsed_time(e[1]) for e in ev), world)
+    ms_step = dist_max(statistics.median(e[0].elapsed_time(e[1]) for e in ev), world)
     peaks = load_peaks()
     value = world * flops / (ms_step * 1e-3) / 1e12
     line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -609,30 +991,39 @@ def size_oracle_sample(layers64, target_s):
     return int(max(8, min(layers64[0][0].total_q, target_s / per_row)))
 
 
+def oracle_sample_calls():
+    """The calls the CPU oracle times, on the host: chunks 0, 10, 21 and 31 of
+    the 16k prefill's first full-causal and first window-128 layer (the same
+    seeded tensors as layers 0 and 1 of the GPU run)."""
+    from gqa_flash_attention_prefill_gb300 import workloads as W
+    st = W.oss20b_stack(num_layers=2, seq=SEQ, chunk_len=CHUNK, seed=3, device="cpu")
+    return [st.call(c, layer) for c in (0, 10, 21, 31) for layer in (0, 1)]
+
+
+SAMPLE_DESC = ("evenly spaced query rows of each of 8 calls of the 16k prefill (chunks 0, 10, "
+               "21, 31 of a full-causal and a window-128 layer), all 64 heads, fp64 CPU oracle")
+
+
 def cpu_baseline(args):
     import oracle
-    from gqa_flash_attention_prefill_gb300 import workloads as W
     oracle.build()
-    layers_cpu = W.layer_pair(seq=args.seq, seed=1)
-    layers64 = oracle_inputs(layers_cpu)
+    layers64 = oracle_inputs(oracle_sample_calls())
     rows = size_oracle_sample(layers64, args.cpu_seconds)
     t, fl, n = oracle_sample_run(layers64, rows)
     return {"value": fl / t / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": f"{rows} evenly spaced query rows of each layer (of {layers_cpu[0].total_q}), "
-                      f"all {layers_cpu[0].hq} heads; {n} rows in {t:.1f} s; "
-                      f"tokens/s {n / t:.1f}"}
+            "sample": f"{rows} {SAMPLE_DESC}; {n} rows in {t:.1f} s, {fl / t / 1e9:.2f} useful "
+                      f"GFLOP/s; rate of the sample, not extrapolated"}
 
 
 def run_reference(args, rank, world):
-    """The CPU oracle as the reference arm, on this workload's metric."""
+    """The CPU oracle as the reference arm, on this workload's metric: each
+    step a bounded sample of rows of the headline workload's calls."""
     if rank != 0:
         return None
     import oracle
-    from gqa_flash_attention_prefill_gb300 import workloads as W
     oracle.build()
-    layers_cpu = W.layer_pair(seq=args.seq, seed=1)
-    layers64 = oracle_inputs(layers_cpu)
+    layers64 = oracle_inputs(oracle_sample_calls())
     # About --ref-seconds (150 s by default) of oracle work in total, however
     # many steps are asked for.
     per_step_s = max(0.005, min(5.0, args.ref_seconds / max(1, args.steps + args.warmup)))
@@ -646,15 +1037,13 @@ def run_reference(args, rank, world):
         fl_total += fl
     value = fl_total / secs / 1e12
     cores = oracle.num_threads()
-    sample = (f"each step: {rows} evenly spaced query rows of each layer (of "
-              f"{layers_cpu[0].total_q}), all {layers_cpu[0].hq} heads, fp64 CPU oracle")
+    sample = f"each step: {rows} {SAMPLE_DESC}"
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) Q/K/V and sinks; no model weights)",
-            "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": args.seq,
-                       "layers": ["full-causal", "window-128"]},
+            "config": bench_config(world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -664,19 +1053,19 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--seq", type=int, default=4096)
+    ap.add_argument("--seq", type=int, default=4096, help="layer_pair workload: tokens")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="CPU work of the oracle baseline sample (rank 0, N=1)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=150.0,
                     help="--impl reference: total CPU seconds of oracle work over all steps")
-    ap.add_argument("--workload", default="layer_pair",
-                    choices=["layer_pair", "chunked_prefix", "oss20b_16k", "ragged", "ragged_full",
+    ap.add_argument("--workload", default="oss20b_16k",
+                    choices=["oss20b_16k", "layer_pair", "chunked_prefix", "ragged", "ragged_full",
                              "ragged_grid", "short_chunk", "decode"],
-                    help="layer_pair is the headline configuration; the others are "
+                    help="oss20b_16k is the headline configuration; the others are "
                          "supplementary measurements")
     ap.add_argument("--layout", default="window-bounded", choices=["window-bounded", "full-prefix"],
                     help="KV layout of the chunked_prefix and decode workloads")
@@ -696,10 +1085,12 @@ def main():
         line = run_reference(args, rank, world)
     elif args.workload == "ragged_grid":
         line = run_ragged_grid(args, rank, world)
-    elif args.workload != "layer_pair":
+    elif args.workload == "layer_pair":
+        line = run_layer_pair(args, rank, world)
+    elif args.workload != "oss20b_16k":
         line = run_workload(args, rank, world)
     else:
-        line = run_ours(args, rank, world)
+        line = run_oss20b(args, rank, world)
         if rank == 0:
             if world == 1 and not args.no_cpu_baseline:
                 line["cpu_baseline"] = cpu_baseline(args)

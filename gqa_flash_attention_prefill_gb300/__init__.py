@@ -12,12 +12,14 @@ import ctypes
 import os
 from typing import Optional
 
-__all__ = ["load", "gqa_flash_prefill", "gqa_flash_prefill_debug", "prefill",
-           "plan", "force_block_n", "force_q_tiles", "get_device_status", "set_tuning",
+__all__ = ["load", "gqa_flash_prefill", "gqa_flash_prefill_debug", "prefill", "prepare",
+           "PreparedCall",
+           "plan", "force_block_n", "force_q_tiles", "get_device_status", "get_stream_status", "set_tuning",
            "gqa_flash_prefill_splitkv", "splitkv_workspace", "prefill_splitkv",
            "gqa_flash_prefill_splitkv_noalloc", "prefill_splitkv_noalloc",
+           "gqa_flash_prefill_masked", "prefill_masked",
            "NOALLOC_SCRATCH_BYTES", "gqa_flash_prefill_paged", "prefill_paged",
-           "clear_config_cache", "config_block_n", "selftest_timeout", "GQAError",
+           "clear_config_cache", "config_block_n", "selftest_timeout", "selftest_exp2", "GQAError",
            "GQA_F16", "GQA_BF16", "GQA_DEV_TIMEOUT", "GQA_DEV_BAD_METADATA",
            "EXPORTED_SYMBOLS"]
 
@@ -33,6 +35,7 @@ EXPORTED_SYMBOLS = [
     "gqa_prefill_selftest_timeout", "gqa_prefill_force_q_tiles",
     "gqa_flash_prefill_splitkv", "gqa_prefill_splitkv_workspace",
     "gqa_flash_prefill_splitkv_noalloc", "gqa_flash_prefill_paged",
+    "gqa_prefill_get_stream_status", "gqa_flash_prefill_masked", "gqa_prefill_selftest_exp2",
 ]
 NOALLOC_SCRATCH_BYTES = 32 << 20  # the library's file-scope split-KV scratch (gqa_prefill.h)
 
@@ -60,7 +63,9 @@ def load(path: Optional[str] = None):
     global _lib
     if _lib is not None and path is None:
         return _lib
-    p = path or LIB_PATH
+    # GQA_PREFILL_LIB names another build of the same library (used to time
+    # two builds against each other on one machine).
+    p = path or os.environ.get("GQA_PREFILL_LIB") or LIB_PATH
     if not os.path.exists(p):
         raise RuntimeError(
             f"CUDA library {p} is missing: build it with "
@@ -76,6 +81,8 @@ def load(path: Optional[str] = None):
     lib.gqa_flash_prefill_debug.restype = ctypes.c_int
     lib.gqa_flash_prefill_splitkv.argtypes = core[:-1] + [ctypes.c_int, vp, ctypes.c_size_t, vp]
     lib.gqa_flash_prefill_splitkv.restype = ctypes.c_int
+    lib.gqa_flash_prefill_masked.argtypes = core[:18] + [vp, vp, ctypes.c_longlong, vp, fp, vp]
+    lib.gqa_flash_prefill_masked.restype = ctypes.c_int
     lib.gqa_flash_prefill_paged.argtypes = [vp] * 7 + [ctypes.c_int] * 10 + [
         ctypes.c_float, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]
     lib.gqa_flash_prefill_paged.restype = ctypes.c_int
@@ -92,6 +99,11 @@ def load(path: Optional[str] = None):
     lib.gqa_prefill_force_q_tiles.restype = ctypes.c_int
     lib.gqa_prefill_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
     lib.gqa_prefill_get_device_status.restype = ctypes.c_int
+    lib.gqa_prefill_get_stream_status.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)]
+    lib.gqa_prefill_get_stream_status.restype = ctypes.c_int
+    lib.gqa_prefill_selftest_exp2.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                              ctypes.c_void_p]
+    lib.gqa_prefill_selftest_exp2.restype = ctypes.c_int
     lib.gqa_prefill_status_string.argtypes = [ctypes.c_int]
     lib.gqa_prefill_status_string.restype = ctypes.c_char_p
     lib.gqa_prefill_version.argtypes = []
@@ -169,6 +181,42 @@ def gqa_flash_prefill(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, scale,
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_flash_prefill")
     return out
+
+
+def gqa_flash_prefill_masked(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, scale,
+                             custom_mask, mask_indptr, window=0, sinks=None,
+                             smooth_softmax=False, out=None, lse=None, stream=None,
+                             max_seqlen_q=0):
+    """gqa_flash_prefill with a custom mask (see gqa_prefill.h): custom_mask
+    is a device tensor of 32-bit words (int32 or uint32), mask_indptr a
+    device int32 [B+1] of word offsets."""
+    for name, t in (("custom_mask", custom_mask), ("mask_indptr", mask_indptr)):
+        if t.element_size() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous tensor of 32-bit words")
+    a = _args(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, scale, window, sinks,
+              smooth_softmax, out, lse, stream, max_seqlen_q)
+    rc = load().gqa_flash_prefill_masked(*a[:18], _ptr(custom_mask), _ptr(mask_indptr),
+                                         int(custom_mask.numel()), *a[18:])
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_flash_prefill_masked")
+    return out
+
+
+def prefill_masked(batch, custom_mask, mask_indptr, out=None, lse=None, with_lse=True,
+                   stream=None):
+    """gqa_flash_prefill_masked on one ``workloads.Batch`` already on the GPU
+    (custom_mask / mask_indptr from ``workloads.pack_custom_mask``, on the
+    GPU); allocates out/lse with torch when not given.  Returns (out, lse)."""
+    import torch
+    if out is None:
+        out = torch.empty_like(batch.q)
+    if lse is None and with_lse:
+        lse = torch.empty(batch.q.shape[:2], dtype=torch.float32, device=batch.q.device)
+    gqa_flash_prefill_masked(batch.q, batch.k, batch.v, batch.cu_seqlens_q, batch.prefix_lens,
+                             batch.kv_indptr, batch.scale, custom_mask, mask_indptr,
+                             window=batch.window, sinks=batch.sinks, smooth_softmax=batch.smooth,
+                             out=out, lse=lse, stream=stream, max_seqlen_q=batch.max_seqlen_q)
+    return out, lse
 
 
 def gqa_flash_prefill_debug(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, scale,
@@ -321,6 +369,34 @@ def prefill(batch, out=None, lse=None, with_lse=True, stream=None):
     return out, lse
 
 
+class PreparedCall:
+    """gqa_flash_prefill with its arguments marshalled once: calling the
+    object re-issues the same C ABI call (same buffers, same stream), which
+    keeps the host cost of a call to the ctypes round trip.  For callers that
+    replay a fixed sequence of calls over resident buffers, such as the
+    layers of a prefill."""
+
+    __slots__ = ("_fn", "_args", "out", "lse")
+
+    def __init__(self, batch, out, lse=None, stream=None):
+        self._fn = load().gqa_flash_prefill
+        self._args = _args(batch.q, batch.k, batch.v, batch.cu_seqlens_q, batch.prefix_lens,
+                           batch.kv_indptr, batch.scale, batch.window, batch.sinks,
+                           batch.smooth, out, lse, stream, batch.max_seqlen_q)
+        self.out, self.lse = out, lse
+
+    def __call__(self):
+        rc = self._fn(*self._args)
+        if rc != GQA_OK:
+            raise GQAError(rc, "gqa_flash_prefill")
+
+
+def prepare(batch, out, lse=None, stream=None) -> PreparedCall:
+    """A PreparedCall of one ``workloads.Batch`` already on the GPU, writing
+    ``out`` (and ``lse`` when given) on ``stream``."""
+    return PreparedCall(batch, out, lse, stream)
+
+
 def plan(num_seqs, total_q, max_seqlen_q, hq, hkv, d, dtype, window) -> dict:
     """Host-only launch plan (rows_per_unit, block_n, kv_stages, ctas_per_sm,
     grid, max_units, q_tiles) for a call with these shapes."""
@@ -378,6 +454,27 @@ def selftest_timeout(timeout_ms: int = 50, stream=None) -> int:
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_prefill_selftest_timeout")
     return st.value
+
+
+def get_stream_status(stream=None) -> int:
+    """Read and clear the device status word in the order of ``stream``
+    (default: the current stream), waiting for that stream only."""
+    v = ctypes.c_int(0)
+    rc = load().gqa_prefill_get_stream_status(_stream_handle(stream), ctypes.byref(v))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_prefill_get_stream_status")
+    return v.value
+
+
+def selftest_exp2(x, stream=None):
+    """2^x through the softmax's FMA-pipe exponential (x: float32 CUDA tensor)."""
+    import torch
+    x = x.contiguous()
+    y = torch.empty_like(x)
+    rc = load().gqa_prefill_selftest_exp2(_ptr(x), _ptr(y), int(x.numel()), _stream_handle(stream))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_prefill_selftest_exp2")
+    return y
 
 
 def get_device_status() -> int:

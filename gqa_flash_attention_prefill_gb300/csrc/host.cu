@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -19,6 +20,27 @@ namespace gqa {
 
 // Device status word (GQA_DEV_* bits); kernels receive its address.
 __device__ unsigned int g_device_status;
+
+// Snapshots of the status word taken by status_take_kernel, one slot per
+// concurrent reader (slots are handed out round-robin).
+constexpr int kStatusSlots = 64;
+__device__ unsigned int g_status_snapshot[kStatusSlots];
+
+// Reads and clears the status word in one atomic step, in stream order.
+__global__ void status_take_kernel(unsigned int* status, unsigned int* snapshot) {
+  *snapshot = atomicExch(status, 0u);
+}
+
+// Evaluates the softmax's FMA-pipe 2^x (exp2_pair_fma) on n inputs, so that
+// it can be checked against exp2 on the device.
+__global__ void selftest_exp2_kernel(const float* x, float* y, int n) {
+  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  float a = x[i], b = (i + 1 < n) ? x[i + 1] : 0.f;
+  exp2_pair_fma(a, b);
+  y[i] = a;
+  if (i + 1 < n) y[i + 1] = b;
+}
 
 // Failure-detection self-test: one thread waits on an mbarrier that nothing
 // ever arrives on, through the same bounded wait the prefill kernel uses.  The
@@ -46,6 +68,7 @@ struct DeviceInfo {
   int sms = 0;
   int smem_per_sm = 0;
   unsigned int* status = nullptr;
+  void* ctx = nullptr;  // the CUDA context the entry belongs to
 };
 std::map<int, DeviceInfo> g_devices;
 
@@ -86,6 +109,34 @@ unsigned long long timeout_ns() {
   return v;
 }
 
+}  // namespace
+
+void* current_context() {
+  typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+  static CtxGetCurrentFn fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<CtxGetCurrentFn>(ptr);
+    return static_cast<CtxGetCurrentFn>(nullptr);
+  }();
+  CUcontext ctx = nullptr;
+  if (fn == nullptr || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+  return ctx;
+}
+
+bool pdl_enabled() {
+  static const bool v = [] {
+    const char* e = std::getenv("GQA_PREFILL_PDL");
+    return !(e != nullptr && e[0] == '0');
+  }();
+  return v;
+}
+
+namespace {
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -109,10 +160,18 @@ EncodeTiledFn encode_fn() {
 int device_info(DeviceInfo* out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
+  void* ctx = current_context();
   std::lock_guard<std::mutex> lk(g_dev_mu);
   auto itr = g_devices.find(dev);
+  // A context other than the one the entry was made in (the device was reset
+  // since) may have loaded the module elsewhere: look everything up again.
+  if (itr != g_devices.end() && itr->second.ctx != ctx) {
+    g_devices.erase(itr);
+    itr = g_devices.end();
+  }
   if (itr == g_devices.end()) {
     DeviceInfo di;
+    di.ctx = ctx;
     if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return GQA_ERR_CUDA;
     if (cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
@@ -121,6 +180,11 @@ int device_info(DeviceInfo* out) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return GQA_ERR_CUDA;
     di.status = static_cast<unsigned int*>(ptr);
+    // Load the status reader's module now: a kernel loaded lazily at its
+    // first launch can wait for work already running on other streams,
+    // which a stream-scoped status read must not do.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, status_take_kernel) != cudaSuccess) return GQA_ERR_CUDA;
     itr = g_devices.emplace(dev, di).first;
   }
   *out = itr->second;
@@ -147,6 +211,7 @@ struct Plan {
   int unit_rows;  // query positions per unit (q_tiles * rows)
   int G, ctas_per_sm, grid, max_units;
   int slots;      // CTAs resident at once (SMs x CTAs per SM)
+  int groups;     // launches: sequences are taken kMaxSeqs at a time
   unsigned smem_launch;  // dynamic smem requested per CTA
 };
 
@@ -164,6 +229,14 @@ constexpr int kMaxSplits = 16;
 struct KvPaging {
   const int32_t* indices = nullptr;
   int page_size = 0, num_pages = 0;
+};
+
+// Custom mask: the per-sequence bitmaps over the extend keys (custom_mask
+// == nullptr: none).
+struct MaskArgs {
+  const uint32_t* custom_mask = nullptr;
+  const int32_t* mask_indptr = nullptr;
+  long long total_words = 0;
 };
 
 struct SplitLayout {
@@ -225,7 +298,9 @@ int make_plan_bn(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, i
   if (d != 64 && d != 128 && d != 256) return GQA_ERR_UNSUPPORTED;
   const int G = Hq / Hkv;
   if (G > 128 || 128 % G != 0) return GQA_ERR_UNSUPPORTED;
-  if (num_seqs > kMaxSeqs) return GQA_ERR_UNSUPPORTED;
+  // Calls with more sequences run as launches over groups of kMaxSeqs.
+  const int seqs_per_launch = num_seqs < kMaxSeqs ? num_seqs : kMaxSeqs;
+  pl->groups = num_seqs > kMaxSeqs ? (num_seqs + kMaxSeqs - 1) / kMaxSeqs : 1;
   DeviceInfo di;
   const bool have_dev = device_info(&di) == GQA_OK;
   int bn = force_bn, qt = force_qt;
@@ -249,9 +324,9 @@ int make_plan_bn(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, i
   pl->G = G;
   pl->rows = 128 / G;
   pl->unit_rows = pl->shape.q_tiles * pl->rows;
-  const long long max_units =
-      (long long)Hkv * ((total_q + pl->unit_rows - 1) / pl->unit_rows + (long long)num_seqs);
-  if (max_units > (1ll << 30)) return GQA_ERR_UNSUPPORTED;
+  const long long max_units =  // per launch
+      (long long)Hkv * ((total_q + pl->unit_rows - 1) / pl->unit_rows + (long long)seqs_per_launch);
+  if (max_units > (1ll << 30) || max_units * pl->groups > (1ll << 30)) return GQA_ERR_UNSUPPORTED;
   pl->max_units = (int)max_units;
   const int by_tmem = 512 / pl->shape.tmem_cols;
   int by_smem = pl->shape.min_blocks;
@@ -346,7 +421,8 @@ int launch_planned(const Plan& pl, const void* q, const void* k, const void* v,
                    const int32_t* kv_indptr, int num_seqs, int total_q, int total_kv, int Hq,
                    int Hkv, int d, int dtype, float scale, int window, const float* sinks,
                    int smooth_softmax, void* out, float* lse, void* stream, int32_t* unit_log,
-                   const SplitArgs& sp = SplitArgs(), const KvPaging& pg = KvPaging()) {
+                   const SplitArgs& sp = SplitArgs(), const KvPaging& pg = KvPaging(),
+                   int first_seq = 0, const MaskArgs& mk = MaskArgs()) {
   DeviceInfo di;
   if (device_info(&di) != GQA_OK) return GQA_ERR_CUDA;
 
@@ -372,6 +448,7 @@ int launch_planned(const Plan& pl, const void* q, const void* k, const void* v,
   p.unit_log = unit_log;
   p.status = di.status;
   p.num_seqs = num_seqs;
+  p.first_seq = first_seq;
   p.total_q = total_q;
   p.total_kv = total_kv;
   p.Hq = Hq;
@@ -386,6 +463,9 @@ int launch_planned(const Plan& pl, const void* q, const void* k, const void* v,
   p.page_size = pg.page_size;
   p.num_pages = pg.num_pages;
   p.page_rows = kv_box;
+  p.custom_mask = mk.custom_mask;
+  p.mask_indptr = mk.mask_indptr;
+  p.total_mask_words = mk.total_words;
   p.num_splits = sp.num_splits > 1 ? sp.num_splits : 1;
   p.part_o = sp.part_o;
   p.part_ml = sp.part_ml;
@@ -399,7 +479,9 @@ int launch_planned(const Plan& pl, const void* q, const void* k, const void* v,
   const bool bf16 = dtype == GQA_BF16;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (paged)
+  if (mk.custom_mask != nullptr)
+    e = launch_mask(p, pl.shape, d, win, bf16, grid, pl.smem_launch, st);
+  else if (paged)
     e = launch_paged(p, pl.shape, d, win, bf16, grid, pl.smem_launch, st);
   else if (p.num_splits > 1)
     e = launch_split(p, pl.shape, d, win, bf16, grid, pl.smem_launch, st);
@@ -420,6 +502,33 @@ int launch_planned(const Plan& pl, const void* q, const void* k, const void* v,
                  pl.shape.q_tiles, pl.shape.kv_stages, grid, pl.ctas_per_sm, pl.max_units,
                  e == cudaSuccess ? "launched" : cudaGetErrorString(e));
   return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+// Launches a planned call group by group: group i takes sequences
+// [i kMaxSeqs, (i+1) kMaxSeqs) through metadata pointers offset to its first
+// sequence (row indices stay absolute), and its unit records start at record
+// i * max_units.  Launches follow each other in stream order, so split-KV
+// groups reuse one workspace.
+int launch_groups(const Plan& pl, const void* q, const void* k, const void* v,
+                  const int32_t* cu_seqlens_q, const int32_t* prefix_lens,
+                  const int32_t* kv_indptr, int num_seqs, int total_q, int total_kv, int Hq,
+                  int Hkv, int d, int dtype, float scale, int window, const float* sinks,
+                  int smooth_softmax, void* out, float* lse, void* stream, int32_t* unit_log,
+                  const SplitArgs& sp = SplitArgs(), const KvPaging& pg = KvPaging(),
+                  const MaskArgs& mk = MaskArgs()) {
+  for (int gi = 0; gi < pl.groups; ++gi) {
+    const int b0 = gi * kMaxSeqs;
+    const int nb = num_seqs - b0 < kMaxSeqs ? num_seqs - b0 : kMaxSeqs;
+    int32_t* log = unit_log != nullptr ? unit_log + 8 * (size_t)gi * pl.max_units : nullptr;
+    MaskArgs mg = mk;
+    if (mg.mask_indptr != nullptr) mg.mask_indptr += b0;
+    const int rc = launch_planned(pl, q, k, v, cu_seqlens_q + b0, prefix_lens + b0,
+                                  kv_indptr + b0, nb, total_q, total_kv, Hq, Hkv, d, dtype, scale,
+                                  window, sinks, smooth_softmax, out, lse, stream, log, sp, pg, b0,
+                                  mg);
+    if (rc != GQA_OK) return rc;
+  }
+  return GQA_OK;
 }
 
 int tune_mode() {
@@ -459,9 +568,9 @@ int tune_key(const void* q, const void* k, const void* v, const int32_t* cu_seql
     rc = make_plan_bn(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, bn, qt, &pl);
     if (rc != GQA_OK) break;
     auto once = [&]() {
-      return launch_planned(pl, q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs, total_q,
-                            total_kv, Hq, Hkv, d, dtype, scale, window, nullptr, 0, out, lse,
-                            stream, nullptr);
+      return launch_groups(pl, q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs, total_q,
+                           total_kv, Hq, Hkv, d, dtype, scale, window, nullptr, 0, out, lse,
+                           stream, nullptr);
     };
     if ((rc = once()) != GQA_OK) break;
     cudaEventRecord(e0, st);
@@ -530,7 +639,7 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q
         int total_kv, int max_seqlen_q, int Hq, int Hkv, int d, int dtype, float scale,
         int window, const float* sinks, int smooth_softmax, void* out, float* lse, void* stream,
         int32_t* unit_log, int num_splits = 1, void* workspace = nullptr,
-        size_t workspace_bytes = 0) {
+        size_t workspace_bytes = 0, ScratchFn scratch = nullptr) {
   if (num_splits < 0 || num_splits > kMaxSplits) return GQA_ERR_INVALID;
   if (num_seqs < 0 || total_q < 0 || total_kv < 0 || max_seqlen_q < 0) return GQA_ERR_INVALID;
   if (Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return GQA_ERR_INVALID;
@@ -569,6 +678,11 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q
   if (rc != GQA_OK) return rc;
   if (sp.num_splits > 1) {
     const SplitLayout L = split_layout(pl, d, sp.num_splits);
+    if (workspace == nullptr && scratch != nullptr) {
+      // The library's own scratch, checked against this very plan's layout.
+      const int rs = scratch(L.bytes, &workspace, &workspace_bytes);
+      if (rs != GQA_OK) return rs;
+    }
     if (workspace == nullptr || workspace_bytes < L.bytes ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
       return GQA_ERR_INVALID;
@@ -577,9 +691,9 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q
     sp.part_ml = reinterpret_cast<float*>(base + L.ml_off);
     sp.part_hdr = reinterpret_cast<int32_t*>(base + L.hdr_off);
   }
-  return launch_planned(pl, q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs, total_q,
-                        total_kv, Hq, Hkv, d, dtype, scale, window, sinks, smooth_softmax, out, lse,
-                        stream, unit_log, sp);
+  return launch_groups(pl, q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs, total_q,
+                       total_kv, Hq, Hkv, d, dtype, scale, window, sinks, smooth_softmax, out, lse,
+                       stream, unit_log, sp);
 }
 
 // Paged KV: the same validation as run(), the pool geometry checks, and a
@@ -623,12 +737,64 @@ int run_paged(const void* q, const void* k_pages, const void* v_pages,
   pg.indices = kv_page_indices;
   pg.page_size = page_size;
   pg.num_pages = num_pages;
-  return launch_planned(pl, q, k_pages, v_pages, cu_seqlens_q, prefix_lens, kv_page_indptr,
-                        num_seqs, total_q, num_page_entries, Hq, Hkv, d, dtype, scale, window,
-                        sinks, smooth_softmax, out, lse, stream, nullptr, SplitArgs(), pg);
+  return launch_groups(pl, q, k_pages, v_pages, cu_seqlens_q, prefix_lens, kv_page_indptr,
+                       num_seqs, total_q, num_page_entries, Hq, Hkv, d, dtype, scale, window,
+                       sinks, smooth_softmax, out, lse, stream, nullptr, SplitArgs(), pg);
+}
+
+// Custom mask: the same validation as run(), the mask arguments, and a plan
+// whose shape has a custom-mask instantiation.
+int run_masked(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+               const int32_t* prefix_lens, const int32_t* kv_indptr, int num_seqs, int total_q,
+               int total_kv, int max_seqlen_q, int Hq, int Hkv, int d, int dtype, float scale,
+               int window, const float* sinks, int smooth_softmax, const uint32_t* custom_mask,
+               const int32_t* mask_indptr, long long total_mask_words, void* out, float* lse,
+               void* stream) {
+  if (num_seqs < 0 || total_q < 0 || total_kv < 0 || max_seqlen_q < 0 || total_mask_words < 0)
+    return GQA_ERR_INVALID;
+  if (Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return GQA_ERR_INVALID;
+  if (dtype != GQA_F16 && dtype != GQA_BF16) return GQA_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return GQA_ERR_INVALID;
+  if (sinks != nullptr && smooth_softmax != 0) return GQA_ERR_INVALID;
+  if (num_seqs == 0 || total_q == 0) return GQA_OK;  // no work, no launch
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr ||
+      cu_seqlens_q == nullptr || prefix_lens == nullptr || kv_indptr == nullptr ||
+      custom_mask == nullptr || mask_indptr == nullptr)
+    return GQA_ERR_INVALID;
+  if (total_kv == 0) return GQA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(custom_mask) & 3u) != 0)
+    return GQA_ERR_INVALID;
+  if (d != 64 && d != 128 && d != 256) return GQA_ERR_UNSUPPORTED;
+  Plan pl;
+  int rc = make_plan(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, &pl);
+  if (rc != GQA_OK) return rc;
+  if (!split_shape(d, pl.shape.block_n, pl.shape.q_tiles)) {
+    const int bn = split_shape(d, pl.shape.block_n, 1) ? pl.shape.block_n : (d == 64 ? 128 : 64);
+    rc = make_plan_bn(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, bn, 1, &pl);
+    if (rc != GQA_OK) return rc;
+  }
+  MaskArgs mk;
+  mk.custom_mask = custom_mask;
+  mk.mask_indptr = mask_indptr;
+  mk.total_words = total_mask_words;
+  return launch_groups(pl, q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs, total_q,
+                       total_kv, Hq, Hkv, d, dtype, scale, window, sinks, smooth_softmax, out, lse,
+                       stream, nullptr, SplitArgs(), KvPaging(), mk);
 }
 
 }  // namespace
+
+int run_splitkv_scratch(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                        const int32_t* prefix_lens, const int32_t* kv_indptr, int num_seqs,
+                        int total_q, int total_kv, int max_seqlen_q, int Hq, int Hkv, int d,
+                        int dtype, float scale, int window, const float* sinks,
+                        int smooth_softmax, void* out, float* lse, int num_splits, void* stream,
+                        ScratchFn scratch) {
+  return run(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs, total_q, total_kv,
+             max_seqlen_q, Hq, Hkv, d, dtype, scale, window, sinks, smooth_softmax, out, lse,
+             stream, nullptr, num_splits, nullptr, 0, scratch);
+}
 
 bool kernel_shape(int d, int block_n, int q_tiles, KernelShape* out) {
   KernelShape s;
@@ -708,6 +874,19 @@ int gqa_flash_prefill_paged(const void* q, const void* k_pages, const void* v_pa
                         smooth_softmax, out, lse, stream);
 }
 
+int gqa_flash_prefill_masked(const void* q, const void* k, const void* v,
+                             const int32_t* cu_seqlens_q, const int32_t* prefix_lens,
+                             const int32_t* kv_indptr, int num_seqs, int total_q, int total_kv,
+                             int max_seqlen_q, int Hq, int Hkv, int d, int dtype, float scale,
+                             int window, const float* sinks, int smooth_softmax,
+                             const uint32_t* custom_mask, const int32_t* mask_indptr,
+                             long long total_mask_words, void* out, float* lse, void* stream) {
+  return gqa::run_masked(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs, total_q,
+                         total_kv, max_seqlen_q, Hq, Hkv, d, dtype, scale, window, sinks,
+                         smooth_softmax, custom_mask, mask_indptr, total_mask_words, out, lse,
+                         stream);
+}
+
 int gqa_prefill_splitkv_workspace(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv,
                                   int d, int dtype, int window, int num_splits, int* splits_used,
                                   size_t* bytes) {
@@ -736,7 +915,7 @@ int gqa_prefill_plan(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hk
   plan->kv_stages = pl.shape.kv_stages;
   plan->ctas_per_sm = pl.ctas_per_sm;
   plan->grid = pl.grid;
-  plan->max_units = pl.max_units;
+  plan->max_units = pl.max_units * pl.groups;  // unit records over all launches
   return GQA_OK;
 }
 
@@ -784,6 +963,15 @@ int gqa_prefill_selftest_timeout(int timeout_ms, void* stream, int* status) {
   return gqa_prefill_get_device_status(status);
 }
 
+int gqa_prefill_selftest_exp2(const float* x, float* y, int n, void* stream) {
+  if (n < 0 || (n > 0 && (x == nullptr || y == nullptr))) return GQA_ERR_INVALID;
+  if (n == 0) return GQA_OK;
+  const int pairs = (n + 1) / 2;
+  gqa::selftest_exp2_kernel<<<(pairs + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      x, y, n);
+  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
 int gqa_prefill_force_block_n(int block_n) {
   if (block_n != 0 && block_n != 64 && block_n != 96 && block_n != 128) return GQA_ERR_INVALID;
   std::lock_guard<std::mutex> lk(gqa::g_mu);
@@ -805,6 +993,26 @@ int gqa_prefill_get_device_status(int* status) {
   if (cudaMemcpyFromSymbol(&v, gqa::g_device_status, sizeof(v)) != cudaSuccess) return GQA_ERR_CUDA;
   if (cudaMemcpyToSymbol(gqa::g_device_status, &zero, sizeof(zero)) != cudaSuccess)
     return GQA_ERR_CUDA;
+  *status = (int)v;
+  return GQA_OK;
+}
+
+int gqa_prefill_get_stream_status(void* stream, int* status) {
+  if (status == nullptr) return GQA_ERR_INVALID;
+  gqa::DeviceInfo di;
+  if (gqa::device_info(&di) != GQA_OK) return GQA_ERR_CUDA;
+  static std::atomic<unsigned> next_slot{0};
+  const unsigned slot = next_slot.fetch_add(1u, std::memory_order_relaxed) % gqa::kStatusSlots;
+  void* snap_base = nullptr;
+  if (cudaGetSymbolAddress(&snap_base, gqa::g_status_snapshot) != cudaSuccess) return GQA_ERR_CUDA;
+  unsigned int* snap = static_cast<unsigned int*>(snap_base) + slot;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  gqa::status_take_kernel<<<1, 1, 0, st>>>(di.status, snap);
+  if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpyAsync(&v, snap, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return GQA_ERR_CUDA;
   *status = (int)v;
   return GQA_OK;
 }

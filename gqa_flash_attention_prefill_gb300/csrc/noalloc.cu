@@ -18,21 +18,35 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+// Device address of the array, looked up once per device and context: the
+// name g_noalloc_scratch is a host-side stand-in in host code, never an
+// address a kernel may be given.  A new context (after a device reset) may
+// hold the module elsewhere, so the address is looked up again then.
+struct ScratchAddr {
+  void* ctx = nullptr;
+  void* addr = nullptr;
+};
 std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices];  // device address of the array, per device
+ScratchAddr g_scratch_addr[kMaxDevices];
 
-// Address of the scratch array on the current device, looked up once.
-int scratch_address(void** addr) {
+// ScratchFn for run_splitkv_scratch: declines a need above the array's size,
+// else hands out the array's device address on the current device.
+int scratch_for(size_t bytes, void** ptr, size_t* capacity) {
+  if (bytes > kNoAllocScratchBytes) return GQA_ERR_UNSUPPORTED;  // declined: too large
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
+  void* ctx = current_context();
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  ScratchAddr& e = g_scratch_addr[dev];
+  if (e.addr == nullptr || e.ctx != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
       return GQA_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+    e.addr = p;
+    e.ctx = ctx;
   }
-  *addr = g_scratch_addr[dev];
+  *ptr = e.addr;
+  *capacity = kNoAllocScratchBytes;
   return GQA_OK;
 }
 
@@ -48,22 +62,16 @@ int gqa_flash_prefill_splitkv_noalloc(const void* q, const void* k, const void* 
                                       int dtype, float scale, int window, const float* sinks,
                                       int smooth_softmax, void* out, float* lse, int num_splits,
                                       void* stream) {
-  if (num_seqs == 0 || total_q == 0) return GQA_OK;  // no work, no launch
-  int splits = 1;
-  size_t bytes = 0;
-  int rc = gqa_prefill_splitkv_workspace(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype,
-                                         window, num_splits, &splits, &bytes);
-  if (rc != GQA_OK) return rc;
-  if (bytes > gqa::kNoAllocScratchBytes) return GQA_ERR_UNSUPPORTED;  // declined: too large
-  void* scratch = nullptr;
-  if (splits > 1 && (rc = gqa::scratch_address(&scratch)) != GQA_OK) return rc;
-  // Nothing in the scratch has to start at zero: every value the merge reads
-  // (unit count, unit headers, each split's (m, l) record and, for non-empty
-  // splits, its partial O) is written earlier in the same call.
-  return gqa_flash_prefill_splitkv(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs,
-                                   total_q, total_kv, max_seqlen_q, Hq, Hkv, d, dtype, scale,
-                                   window, sinks, smooth_softmax, out, lse, splits, scratch,
-                                   splits > 1 ? gqa::kNoAllocScratchBytes : 0, stream);
+  // The same validation, plan and launch as gqa_flash_prefill_splitkv; when
+  // the plan splits, the scratch comes from scratch_for, which checks the
+  // plan's own workspace layout against the array.  Nothing in the scratch
+  // has to start at zero: every value the merge reads (unit count, unit
+  // headers, each split's (m, l) record and, for non-empty splits, its
+  // partial O) is written earlier in the same call.
+  return gqa::run_splitkv_scratch(q, k, v, cu_seqlens_q, prefix_lens, kv_indptr, num_seqs,
+                                  total_q, total_kv, max_seqlen_q, Hq, Hkv, d, dtype, scale,
+                                  window, sinks, smooth_softmax, out, lse, num_splits, stream,
+                                  gqa::scratch_for);
 }
 
 }  // extern "C"

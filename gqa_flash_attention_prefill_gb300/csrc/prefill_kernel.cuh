@@ -33,7 +33,8 @@
 
 namespace gqa {
 
-constexpr int kMaxSeqs = 512;        // sequences per call (shared-memory tables)
+constexpr int kMaxSeqs = 512;        // sequences per launch (shared-memory tables)
+constexpr int kSortSeqs = 64;        // launches with at most this many sequences deal them costliest first
 // Threads per CTA with QT query tiles: a softmax warpgroup per tile, one
 // producer warp and one MMA warp.
 __host__ __device__ constexpr int threads_for(int QT) { return 32 * (4 * QT + 2); }
@@ -59,6 +60,12 @@ struct PrefillParams {
   int32_t* unit_log;
   unsigned int* status;
   int num_seqs, total_q, total_kv;
+  // Index of this launch's first sequence in the caller's batch: a call with
+  // more sequences than the shared-memory tables hold runs as several
+  // launches over consecutive groups of sequences, each given metadata
+  // pointers offset to its group.  cu_seqlens_q[0] == 0 is checked only in
+  // the first group.
+  int first_seq;
   int Hq, Hkv, G, rows;  // rows = query positions per 128-row query tile = 128 / G
   int window;            // <= 0: none
   int smooth;
@@ -77,6 +84,13 @@ struct PrefillParams {
   // boxes of page_rows = min(BN, page_size) rows.
   const int32_t* kv_page_indices;
   int page_size, num_pages, page_rows;
+  // Custom mask (the MASK instantiation): per sequence a bitmap over its
+  // extend keys, ANDed with the causal and window conditions; row i of
+  // sequence b holds words custom_mask[mask_indptr[b] + i W ..] with
+  // W = ceil(E / 32), extend key j' at bit j' % 32 of word j' / 32.
+  const uint32_t* custom_mask;
+  const int32_t* mask_indptr;
+  long long total_mask_words;
 };
 
 __host__ __device__ constexpr int pow2_cols(int n) {
@@ -97,6 +111,18 @@ __host__ __device__ constexpr int tmem_alloc_for(int D, int BN, int QT) {
   return QT == 1 ? tmem_cols_for(D, BN) : 512;
 }
 
+// Columns of each 64-column chunk whose exponentials go to the FMA pipe
+// (exp2_pair_fma) on tiles without a mask, for the shapes where the
+// special-function unit's ex2 rate limits the softmax: head dim 64 with
+// 128-key tiles (the full-causal default).  GQA_EMU_COLS overrides it for
+// measurements.
+#ifndef GQA_EMU_COLS
+#define GQA_EMU_COLS 0
+#endif
+__host__ __device__ constexpr int emu_cols(int D, int BN) {
+  return (D == 64 && BN == 128) ? GQA_EMU_COLS : 0;
+}
+
 // Q tiles in flight per CTA: two for d = 64 (the next unit's Q loads during
 // the current unit and two CTAs still fit on an SM), one for larger d.
 __host__ __device__ constexpr int q_buffers(int D) { return D == 64 ? 2 : 1; }
@@ -107,7 +133,7 @@ __host__ __device__ constexpr uint32_t smem_bytes_for(int D, int BN, int NS, int
          + 2u * NS * BN * D * 2u                        // K and V rings
          + 64u * 8u                                     // mbarriers
          + 16u                                          // misc words
-         + 4u * (4 * kMaxSeqs + 2)                      // per-sequence tables
+         + 4u * (5 * kMaxSeqs + 2)                      // per-sequence tables
          + 4u * 16u;                                    // scan scratch (one word per warp)
 }
 
@@ -132,35 +158,37 @@ struct Unit {
 // Per-sequence metadata copied into shared memory once per CTA, so that
 // decoding a unit never waits on global memory.
 struct SeqTab {
-  const int32_t* tile_start;  // [B+1] exclusive scan of units per sequence
+  const int32_t* tile_start;  // [B+1] exclusive scan of units per sequence, in dealing order
   const int32_t* cu0;         // [B+1] cu_seqlens_q
   const int32_t* pre;         // [B]   prefix_lens
   const int32_t* kvb;         // [B]   kv_indptr (first key row)
+  const int32_t* order;       // [B]   sequence dealt r-th
 };
 
 // Unit u -> (sequence, KV head, unit of `urows` query positions).  Units are
-// numbered with the KV head fastest and, inside a sequence, the last
-// (costliest under causality) unit first.
+// numbered with the KV head fastest, sequences in their dealing order and,
+// inside a sequence, the last (costliest under causality) unit first.
 __device__ __forceinline__ Unit decode_unit(const PrefillParams& p, const SeqTab& T, int u,
                                             int BN, int urows) {
   Unit U;
   U.g = u % p.Hkv;
   const int tau = u / p.Hkv;
-  int lo = 0, hi = p.num_seqs;  // find b with tile_start[b] <= tau < tile_start[b+1]
+  int lo = 0, hi = p.num_seqs;  // find r with tile_start[r] <= tau < tile_start[r+1]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (T.tile_start[mid] <= tau) lo = mid; else hi = mid;
   }
-  U.b = lo;
   const int t = tau - T.tile_start[lo];
   const int tiles_b = T.tile_start[lo + 1] - T.tile_start[lo];
+  const int b = T.order[lo];
+  U.b = b;
   U.q0 = (tiles_b - 1 - t) * urows;
-  U.P = T.pre[lo];
-  const int cu0 = T.cu0[lo];
-  U.E = T.cu0[lo + 1] - cu0;
+  U.P = T.pre[b];
+  const int cu0 = T.cu0[b];
+  U.E = T.cu0[b + 1] - cu0;
   U.q_last = min(U.q0 + urows, U.E) - 1;
   U.q_row0 = cu0 + U.q0;
-  U.kv_base = T.kvb[lo];
+  U.kv_base = T.kvb[b];
   const KvRange r = kv_range(U.P, U.q0, U.q_last, p.window, BN);
   U.kv_lo = r.kv_lo;
   U.n_tiles = r.n_tiles;
@@ -242,6 +270,24 @@ __device__ __forceinline__ void load_kv_tile(const PrefillParams& p, const Unit&
   }
 }
 
+// Custom-mask bits of a 64-key chunk for one query row: bit c is set when key
+// jp0 + c of the extend part (jp0 may be negative: the chunk's first -jp0
+// keys are prefix keys, which the mask does not cover) is kept.  `row` is
+// the row's W words; words past the row's last are never needed (keys past
+// the row's own position are masked causally), so reads clamp to it.
+__device__ __forceinline__ uint64_t custom_keep_bits(const uint32_t* row, int W, int jp0) {
+  if (jp0 + 64 <= 0) return ~0ull;
+  const int lo = jp0 > 0 ? jp0 : 0;
+  const int off = lo - jp0;  // prefix keys at the chunk's start (< 64)
+  const int w0 = lo >> 5, sh = lo & 31;
+  const uint32_t a = __ldg(row + min(w0, W - 1));
+  const uint32_t b = __ldg(row + min(w0 + 1, W - 1));
+  const uint32_t c = __ldg(row + min(w0 + 2, W - 1));
+  uint64_t bits = (((uint64_t)b << 32) | a) >> sh;
+  if (sh != 0) bits |= (uint64_t)c << (64 - sh);
+  return off == 0 ? bits : ((bits << off) | ((1ull << off) - 1ull));
+}
+
 // k-th unit of this CTA: round k of a snake (boustrophedon) deal over the
 // grid, so that with units ordered by decreasing cost every CTA alternates
 // between the expensive and the cheap end of each round.
@@ -301,13 +347,15 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity,
 }
 
 
-// SPL: split-KV work items writing partials; PAGED: K/V from a page pool.
-// Both are separate instantiations, so the default kernel carries none of
-// their code.
-template <int D, int BN, int NS, bool WIN, bool BF16, int MINB, int QT, bool SPL, bool PAGED>
+// SPL: split-KV work items writing partials; PAGED: K/V from a page pool;
+// MASK: the custom mask ANDed into the causal / window mask.  Each is a
+// separate instantiation, so the default kernel carries none of their code.
+template <int D, int BN, int NS, bool WIN, bool BF16, int MINB, int QT, bool SPL, bool PAGED,
+          bool MASK = false>
 __global__ void __launch_bounds__(threads_for(QT), MINB)
     prefill_kernel(const __grid_constant__ PrefillParams p) {
   static_assert(D == 64 || D == 128 || D == 256, "head dim");
+  static_assert(!MASK || (BN != 96 && !SPL && !PAGED && QT == 1), "custom-mask shapes");
   static_assert(BN == 64 || BN == 96 || BN == 128, "key tile");
   static_assert(QT == 1 || (QT == 2 && tmem_cols_for(D, BN) <= 256), "query tiles per CTA");
   constexpr int kThr = threads_for(QT);
@@ -340,8 +388,9 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
   int32_t* seq_cu0 = tile_start + (kMaxSeqs + 1);
   int32_t* seq_pre = seq_cu0 + (kMaxSeqs + 1);
   int32_t* seq_kvb = seq_pre + kMaxSeqs;
-  int32_t* scan = seq_kvb + kMaxSeqs;
-  const SeqTab T{tile_start, seq_cu0, seq_pre, seq_kvb};
+  int32_t* seq_order = seq_kvb + kMaxSeqs;
+  int32_t* scan = seq_order + kMaxSeqs;
+  const SeqTab T{tile_start, seq_cu0, seq_pre, seq_kvb, seq_order};
   volatile uint32_t* abort_flag = misc + 1;
   const unsigned long long tmo = p.timeout_ns;
   const int win = WIN ? p.window : 0;
@@ -372,14 +421,21 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
     tma_prefetch_desc(&p.tmap_v);
   }
   __syncthreads();
+  // Everything above touches only this CTA's own shared memory and the
+  // kernel parameters, so under programmatic dependent launch it overlaps
+  // the previous kernel's tail.  The next kernel in the stream may start its
+  // own set-up as soon as this grid's CTAs finish; nothing below reads
+  // device memory before the previous kernel's writes are visible.
+  grid_dep_launch_dependents();
+  grid_dep_wait();
 
-  // Per-sequence unit counts, their exclusive scan, and the metadata checks
-  // (bad metadata: write nothing, raise GQA_DEV_BAD_METADATA).
+  // Per-sequence tables and metadata checks (bad metadata: write nothing,
+  // raise GQA_DEV_BAD_METADATA), the order in which sequences are dealt, and
+  // the exclusive scan of their unit counts in that order.
   const int nseq = p.num_seqs;
   const int per = (nseq + kThr - 1) / kThr;
   const int b_lo = min(tid * per, nseq), b_hi = min(b_lo + per, nseq);
-  int local = 0;
-  bool bad = (tid == 0) && (__ldg(p.cu_seqlens_q) != 0);
+  bool bad = (tid == 0) && p.first_seq == 0 && (__ldg(p.cu_seqlens_q) != 0);
   for (int b = b_lo; b < b_hi; ++b) {
     const int c0 = __ldg(p.cu_seqlens_q + b), c1 = __ldg(p.cu_seqlens_q + b + 1);
     const int P = __ldg(p.prefix_lens + b);
@@ -388,18 +444,61 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
     // KV rows (contiguous) or pages (paged) of the sequence: exactly P + E keys.
     const long long kv_need =
         PAGED ? ((long long)P + E + p.page_size - 1) / p.page_size : (long long)P + E;
+    int key = -1;  // tiles of the sequence's costliest (last) unit; -1: no units
+    bool mask_bad = false;
+    if constexpr (MASK) {  // the sequence's bitmap: E rows of ceil(E / 32) words
+      const long long m0 = __ldg(p.mask_indptr + b), m1 = __ldg(p.mask_indptr + b + 1);
+      mask_bad = m0 < 0 || m1 > p.total_mask_words ||
+                 m1 - m0 != (long long)E * ((E + 31) / 32);
+    }
     if (E < 0 || P < 0 || c0 < 0 || c1 > p.total_q || k0 < 0 || k1 > p.total_kv ||
-        (long long)k1 - k0 != kv_need)
+        (long long)k1 - k0 != kv_need || mask_bad)
       bad = true;
-    else
-      local += (E + urows - 1) / urows;
+    else if (E > 0)
+      key = kv_range(P, ((E - 1) / urows) * urows, E - 1, win, BN).n_tiles;
     seq_cu0[b] = c0;
     seq_pre[b] = P;
     seq_kvb[b] = k0;
+    seq_order[b] = b;
+    tile_start[b] = key;  // the keys wait here until the scan below
     if (b == nseq - 1) seq_cu0[nseq] = c1;
   }
   if (bad) misc[2] = 1u;
-  // Exclusive scan of the per-thread counts: warp scans, then warp totals.
+  __syncthreads();
+  // Costliest first across the batch: a small batch deals its sequences by
+  // decreasing key (ties by index), so the long units of every sequence go
+  // out before any short one; inside a sequence the units are already dealt
+  // costliest first.  Larger batches keep their own order (the ranking costs
+  // batch-size squared comparisons).
+  if (nseq > 1 && nseq <= kSortSeqs) {
+    int rank[(kSortSeqs + kThr - 1) / kThr];
+#pragma unroll
+    for (int i = 0; i < (kSortSeqs + kThr - 1) / kThr; ++i) {
+      const int b = b_lo + i;
+      rank[i] = 0;
+      if (b < b_hi) {
+        const int kb = tile_start[b];
+        for (int o = 0; o < nseq; ++o) {
+          const int ko = tile_start[o];
+          rank[i] += (ko > kb || (ko == kb && o < b)) ? 1 : 0;
+        }
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < (kSortSeqs + kThr - 1) / kThr; ++i)
+      if (b_lo + i < b_hi) seq_order[rank[i]] = b_lo + i;
+    __syncthreads();
+  }
+  // Units per sequence in dealing order, then their exclusive scan: warp
+  // scans, then warp totals.  tile_start[r] is the first unit (of one KV
+  // head) of the r-th sequence dealt.
+  auto units_of = [&](int b) {
+    const int E = seq_cu0[b + 1] - seq_cu0[b];
+    return E > 0 ? (E + urows - 1) / urows : 0;
+  };
+  int local = 0;
+  for (int r = b_lo; r < b_hi; ++r) local += units_of(seq_order[r]);
   int incl = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -420,10 +519,9 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
   __syncthreads();
   {
     int acc = scan[warp] + incl - local;
-    for (int b = b_lo; b < b_hi; ++b) {
-      tile_start[b] = acc;
-      const int E = __ldg(p.cu_seqlens_q + b + 1) - __ldg(p.cu_seqlens_q + b);
-      acc += E > 0 ? (E + urows - 1) / urows : 0;
+    for (int r = b_lo; r < b_hi; ++r) {
+      tile_start[r] = acc;
+      acc += units_of(seq_order[r]);
     }
   }
   __syncthreads();
@@ -666,6 +764,13 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
       const int pl = q0s + r / p.G;  // query position inside the sequence
       const int h = U.g * p.G + r % p.G;
       const int pos = U.P + pl;
+      const uint32_t* mrow = nullptr;  // this row's custom-mask words
+      int mwords = 0;
+      if constexpr (MASK) {
+        mwords = (U.E + 31) / 32;
+        if (pl <= qls)
+          mrow = p.custom_mask + __ldg(p.mask_indptr + U.b) + (long long)pl * mwords;
+      }
       float m = -INFINITY;  // exponent reference (log2 domain)
       float l = 0.f;        // running denominator, relative to m
       int n_masked = 0;     // tiles of the unit needing the mask (tile_needs_mask)
@@ -683,6 +788,10 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
         // the tile's last position's lower bound).
         const bool edge_c = n0 + BN - 1 > U.P + q0s;
         const bool edge_w = WIN && n0 < U.P + qls - win + 1;
+        const bool edge_m = MASK && n0 + BN - 1 >= U.P;  // the tile reaches the extend keys
+        // No masked score in the tile: every x below is finite and <= 8.
+        const bool interior = !(edge_c || edge_w || edge_m);
+        constexpr int kEmu = (BN != 96) ? emu_cols(D, BN) : 0;
         n_masked += tile_needs_mask(n0, BN, U.P, U.q0, U.q_last, win) ? 1 : 0;
         // S is processed in CW-column chunks (64, or 48 for 96-key tiles).
         constexpr int CW = (BN == 96) ? 48 : 64;
@@ -728,8 +837,16 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
                 if (c < c_lo) sr[c] = __float_as_uint(-INFINITY);
             }
           }
+          if constexpr (MASK) {
+            if (edge_m && mrow != nullptr) {
+              const uint64_t keep = custom_keep_bits(mrow, mwords, n0 + ch * CW - U.P);
+#pragma unroll
+              for (int c = 0; c < CW; ++c)
+                if (!((keep >> c) & 1ull)) sr[c] = __float_as_uint(-INFINITY);
+            }
+          }
           float mx = fmaxf(red0, red1);
-          if (CW != 64 || edge_c || edge_w) {
+          if (CW != 64 || edge_c || edge_w || edge_m) {
             // Masked (or 48-column) chunk: maximum over the kept values, over
             // independent chains (short dependency chains).
             float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
@@ -767,8 +884,13 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
             for (int t = 0; t < 8; t += 2)
               unf2(ffma2(f2(__uint_as_float(sr[c + t]), __uint_as_float(sr[c + t + 1])), sc2, nm2),
                    x[t], x[t + 1]);
+            if (kEmu > c && interior) {
 #pragma unroll
-            for (int t = 0; t < 8; ++t) x[t] = ex2(x[t]);
+              for (int t = 0; t < 8; t += 2) exp2_pair_fma(x[t], x[t + 1]);
+            } else {
+#pragma unroll
+              for (int t = 0; t < 8; ++t) x[t] = ex2(x[t]);
+            }
             acc0 = fadd2(acc0, f2(x[0], x[1]));
             acc1 = fadd2(acc1, f2(x[2], x[3]));
             acc2 = fadd2(acc2, f2(x[4], x[5]));

@@ -96,8 +96,10 @@ enum {
 
 /*
  * gqa_flash_prefill -- the fused prefill (see the definition above).
- *   num_seqs     B >= 0 (at most 512 per call: the kernel keeps every
- *                sequence's metadata in shared memory; more is declined)
+ *   num_seqs     B >= 0.  The kernel keeps each launch's sequence metadata in
+ *                shared memory, 512 sequences at most: a call with more runs
+ *                as ceil(B / 512) launches, in stream order, over consecutive
+ *                groups of 512 sequences.
  *   total_q      rows of q/out (>= cu_seqlens_q[B]); 0 means no work
  *   total_kv     rows of k/v (>= kv_indptr[B])
  *   max_seqlen_q optional host hint, max_b E_b (0 = unknown); only used to
@@ -117,6 +119,45 @@ GQA_API int gqa_flash_prefill(const void* q, const void* k, const void* v,
                       int total_kv, int max_seqlen_q, int Hq, int Hkv, int d,
                       int dtype, float scale, int window, const float* sinks,
                       int smooth_softmax, void* out, float* lse, void* stream);
+
+/*
+ * gqa_flash_prefill_masked -- gqa_flash_prefill with a custom mask ANDed
+ * into the causal and window conditions: one more condition on a key, which
+ * can only remove keys (sgl-project/sglang PR #34468, "gfx950 SWA prefix
+ * trim": the custom mask combined with a sliding window, the EAGLE
+ * target-verify route of commit 1, and the PR body's note that custom-mask
+ * and causal conjuncts can only empty a tile further, so the loop floor is
+ * unchanged).
+ *
+ *   custom_mask       device uint32 words, 4-byte aligned: per sequence a
+ *                     bitmap over its extend keys.  Row i (0 <= i < E_b) of
+ *                     sequence b occupies words mask_indptr[b] + i * W_b ..
+ *                     + W_b - 1, W_b = ceil(E_b / 32); extend key j' (key
+ *                     P_b + j' of the sequence) is kept for row i only if bit
+ *                     j' % 32 of word j' / 32 is set.  Prefix keys are not
+ *                     covered by the bitmap (only the causal and window
+ *                     conditions apply to them); bits above the row's own
+ *                     position are ignored (causality removes those keys).
+ *   mask_indptr       device int32 [num_seqs + 1]: mask_indptr[b + 1] -
+ *                     mask_indptr[b] == E_b * W_b, mask_indptr[0] >= 0.
+ *   total_mask_words  words in custom_mask (>= mask_indptr[num_seqs]).
+ *
+ * A row left with no key gets out = 0 and lse = -inf, as in
+ * gqa_flash_prefill.  Inconsistent mask metadata raises
+ * GQA_DEV_BAD_METADATA like the other metadata.  Head dims, dtypes, sink
+ * modes, windows and KV layouts as gqa_flash_prefill (the contiguous KV
+ * layout only); the key tile is 128 (d = 64, full attention) or 64.
+ * Returns as gqa_flash_prefill; GQA_ERR_INVALID also for a NULL or
+ * misaligned mask.
+ */
+GQA_API int gqa_flash_prefill_masked(const void* q, const void* k, const void* v,
+                                     const int32_t* cu_seqlens_q, const int32_t* prefix_lens,
+                                     const int32_t* kv_indptr, int num_seqs, int total_q,
+                                     int total_kv, int max_seqlen_q, int Hq, int Hkv, int d,
+                                     int dtype, float scale, int window, const float* sinks,
+                                     int smooth_softmax, const uint32_t* custom_mask,
+                                     const int32_t* mask_indptr, long long total_mask_words,
+                                     void* out, float* lse, void* stream);
 
 /*
  * gqa_flash_prefill_paged -- the same operation as gqa_flash_prefill with K
@@ -201,14 +242,18 @@ GQA_API int gqa_flash_prefill_splitkv(const void* q, const void* k, const void* 
  *
  *   num_splits  as gqa_flash_prefill_splitkv (0 = the library's choice).
  *
- * Shapes whose split-KV workspace (gqa_prefill_splitkv_workspace for the same
- * arguments) exceeds the array return GQA_ERR_UNSUPPORTED before any launch.
- * Nothing in the array has to start at zero: every value the merge reads is
- * written earlier in the same call.  The array is one per device and process:
- * calls that overlap in time on a device (other streams, other host threads)
- * race on it, so the caller must order them.  Other arguments, layouts and
- * return codes as gqa_flash_prefill; GQA_ERR_CUDA if the array's address
- * cannot be obtained.
+ * Arguments are validated exactly as gqa_flash_prefill_splitkv does, and with
+ * the same return codes (empty work is GQA_OK only after that validation).
+ * The plan that launches is the plan whose workspace layout is checked:
+ * shapes needing more than the array (gqa_prefill_splitkv_workspace for the
+ * same arguments) return GQA_ERR_UNSUPPORTED before any launch.  Nothing in
+ * the array has to start at zero: every value the merge reads is written
+ * earlier in the same call.  The array is one per device and process: calls
+ * that overlap in time on a device (other streams, other host threads) race
+ * on it, so the caller must order them.  The first splitting call on a
+ * device looks up the array's device address (again after a device reset
+ * creates a new context); make that first call before any stream capture.
+ * GQA_ERR_CUDA if the address cannot be obtained.
  */
 GQA_API int gqa_flash_prefill_splitkv_noalloc(const void* q, const void* k, const void* v,
                                               const int32_t* cu_seqlens_q,
@@ -245,7 +290,8 @@ typedef struct {
     int kv_stages;      /* K/V shared-memory ring depth */
     int ctas_per_sm;    /* resident CTAs per SM the launch assumes */
     int grid;           /* CTAs launched (persistent) */
-    int max_units;      /* upper bound on units: Hkv * (ceil(total_q/rows) + B) */
+    int max_units;      /* upper bound on unit records: Hkv * (ceil(total_q/rows) + B'),
+                           B' = min(B, 512), times the launches ceil(B / 512) */
     int q_tiles;        /* 128-row query tiles per unit: 1, or 2 (one CTA per SM) */
 } gqa_prefill_plan_t;
 
@@ -262,6 +308,9 @@ GQA_API int gqa_prefill_plan(int num_seqs, int total_q, int max_seqlen_q, int Hq
  * kv_lo / n_tiles are the key tiles the unit walked (kv_lo relative to the
  * sequence's first key), n_masked how many of them needed the per-element
  * mask, cta the CTA that ran it and order its position in that CTA's list.
+ * With more than 512 sequences, launch i (sequences from 512 i on) writes its
+ * records from record i * (max_units / launches) on, and its b counts from
+ * that launch's first sequence.
  */
 GQA_API int gqa_flash_prefill_debug(const void* q, const void* k, const void* v,
                             const int32_t* cu_seqlens_q,
@@ -334,6 +383,30 @@ GQA_API int gqa_prefill_selftest_timeout(int timeout_ms, void* stream, int* stat
  * GQA_ERR_CUDA; *status receives the bits.
  */
 GQA_API int gqa_prefill_get_device_status(int* status);
+
+/*
+ * Self-test of the softmax's 2^x on the FMA pipe (used for a fraction of the
+ * exponentials when head dim is 64 and the key tile 128): y[i] = 2^x[i] for
+ * n device floats, enqueued on `stream`, for inputs in [-126, 8] (the range
+ * the softmax passes: scores minus a running maximum, at most 8 above it).
+ * Cody-Waite range reduction and a degree-3 minimax polynomial fitted with
+ * the Remez exchange algorithm; relative error at most 7.5e-5 over that
+ * range.  Returns GQA_OK, GQA_ERR_INVALID or GQA_ERR_CUDA.
+ */
+GQA_API int gqa_prefill_selftest_exp2(const float* x, float* y, int n, void* stream);
+
+/*
+ * gqa_prefill_get_stream_status -- the same status word, read without a
+ * device-wide synchronisation: a one-thread kernel enqueued on `stream`
+ * takes the word and clears it in one atomic exchange, and the call waits
+ * for `stream` only.  *status then holds every bit raised by kernels that
+ * completed before that point of `stream` (in particular all earlier calls
+ * on `stream`), and possibly bits from kernels still running on other
+ * streams; no bit is lost between the read and the clear.  Up to 64 host
+ * threads may read concurrently.  Returns GQA_OK, GQA_ERR_INVALID for a NULL
+ * status, or GQA_ERR_CUDA.
+ */
+GQA_API int gqa_prefill_get_stream_status(void* stream, int* status);
 
 /* Static text for a GQA_* return code. */
 GQA_API const char* gqa_prefill_status_string(int code);

@@ -77,7 +77,7 @@ def _call(lib, **over):
     (dict(total_kv=0), -1),
     (dict(d=96), -2),                   # declined: head dim not implemented
     (dict(hq=24, hkv=1), -2),           # declined: G does not divide 128
-    (dict(B=4096), -2),                 # declined: more sequences than the tile table
+    (dict(B=1 << 22, total_q=1 << 22), -2),  # declined: unit records overflow
 ])
 def test_invalid_arguments_are_rejected_before_launch(lib, over, code):
     assert _call(lib, **over) == code
@@ -87,6 +87,38 @@ def test_empty_work_is_ok_without_launch(lib):
     assert _call(lib, B=0) == 0
     assert _call(lib, total_q=0) == 0
     assert _call(lib, B=0, q=None, k=None, v=None, out=None) == 0
+
+
+def _call_noalloc(lib, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, cu=FAKE, pre=FAKE, kvi=FAKE, B=1, total_q=16,
+             total_kv=16, max_q=16, hq=8, hkv=2, d=64, dtype=1, scale=0.125, window=0,
+             sinks=None, smooth=0, out=FAKE, lse=None, splits=2, stream=None)
+    a.update(over)
+    return lib.gqa_flash_prefill_splitkv_noalloc(
+        a["q"], a["k"], a["v"], a["cu"], a["pre"], a["kvi"], a["B"], a["total_q"],
+        a["total_kv"], a["max_q"], a["hq"], a["hkv"], a["d"], a["dtype"], a["scale"],
+        a["window"], a["sinks"], a["smooth"], a["out"], a["lse"], a["splits"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(hq=6, hkv=4), -1),
+    (dict(dtype=7), -1),
+    (dict(scale=0.0), -1),
+    (dict(sinks=FAKE, smooth=1), -1),
+    (dict(splits=17), -1),
+    (dict(splits=-1), -1),
+    (dict(q=None), -1),
+    (dict(d=96), -2),
+    # arguments are checked before the empty-work early return
+    (dict(B=0, hq=6, hkv=4), -1),
+    (dict(total_q=0, dtype=7), -1),
+    (dict(total_q=0, sinks=FAKE, smooth=1), -1),
+    (dict(B=0, scale=float("nan")), -1),
+    (dict(B=0), 0),
+    (dict(total_q=0), 0),
+])
+def test_noalloc_entry_validates_like_the_others(lib, over, code):
+    assert _call_noalloc(lib, **over) == code
 
 
 def test_plan_is_host_only(lib):
@@ -152,3 +184,31 @@ def test_split_count_choice_is_host_only(lib):
     assert used > 1 and nbytes > 0
     used, nbytes = pkg.splitkv_workspace(1, 64, 64, 64, 8, 64, "bf16", 0, 16)
     assert used == 16 and nbytes > 0
+
+
+def _call_masked(lib, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, cu=FAKE, pre=FAKE, kvi=FAKE, B=1, total_q=16,
+             total_kv=16, max_q=16, hq=8, hkv=2, d=64, dtype=1, scale=0.125, window=0,
+             sinks=None, smooth=0, mask=FAKE, mip=FAKE, words=16, out=FAKE, lse=None,
+             stream=None)
+    a.update(over)
+    return lib.gqa_flash_prefill_masked(
+        a["q"], a["k"], a["v"], a["cu"], a["pre"], a["kvi"], a["B"], a["total_q"],
+        a["total_kv"], a["max_q"], a["hq"], a["hkv"], a["d"], a["dtype"], a["scale"],
+        a["window"], a["sinks"], a["smooth"], a["mask"], a["mip"], a["words"], a["out"],
+        a["lse"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(mask=None), -1),
+    (dict(mip=None), -1),
+    (dict(mask=FAKE + 2), -1),          # words must be 4-byte aligned
+    (dict(words=-1), -1),
+    (dict(hq=6, hkv=4), -1),
+    (dict(sinks=FAKE, smooth=1), -1),
+    (dict(d=96), -2),
+    (dict(B=0), 0),
+    (dict(B=0, dtype=7), -1),
+])
+def test_masked_entry_validates_before_launch(lib, over, code):
+    assert _call_masked(lib, **over) == code

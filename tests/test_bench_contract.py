@@ -48,17 +48,27 @@ def test_gpu_arm_line():
     line = _bench("--steps", "5", "--warmup", "3", "--cpu-seconds", "1")
     _common(line)
     assert line["n_gpus"] == 1 and line["dtype"] == "bf16"
-    rf = line["roofline"]
-    assert rf["bound"] == "tensor" and rf["unit"] == "TFLOP/s"
-    assert 0 < rf["achieved"] and 0 < rf["peak"]
-    assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-3
-    # A number far above the measured peak would mean the kernel skipped work.
-    assert rf["frac"] < 1.2
+    assert line["config"]["calls_per_step"] == 768
+    for key, bound, unit in (("roofline", "tensor", "TFLOP/s"),
+                             ("roofline_window", "hbm", "GB/s")):
+        rf = line[key]
+        assert rf["bound"] == bound and rf["unit"] == unit
+        assert 0 < rf["achieved"] and 0 < rf["peak"]
+        assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-3
+        # A number far above the measured peak would mean the kernel skipped work.
+        assert rf["frac"] < 1.2
+    # the per-kernel pass accounts for the whole step (isolated kernels run
+    # no faster than the step's back-to-back launches)
+    kinds = line["per_kind"]
+    assert kinds["full_causal"]["calls"] == 384 and kinds["window_128"]["calls"] == 384
+    assert sum(k["ms_per_step"] for k in kinds.values()) > 0.9 * line["ms_per_step"]
     e2e = line["e2e"]
-    assert 0 < e2e["value"] < line["value"]
+    assert 0 < e2e["value"] < 1.05 * line["value"]
     assert e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
-    assert line["gpu_launches"] == 2 * line["steps"]
+    assert line["gpu_launches"] == 768 * line["steps"]
     assert "sm_mhz" in line["clocks"] and "reasons" in line["clocks"]
-    assert line["warm_l2"]["value"] > 0
+    pair = line["layer_pair"]
+    assert pair["value"] > 0 and pair["full_causal"]["bound"] == "tensor"
+    assert 0 < pair["window_128"]["frac"] < 1.2 and 0 < pair["full_causal"]["frac"] < 1.2
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1

@@ -85,3 +85,55 @@ def test_non_default_stream(pkg):
     s.synchronize()
     ref, ref_lse = run_oracle(b)
     compare(out.cpu(), lse.cpu(), ref, ref_lse, label="side stream")
+
+
+def test_stream_status_reads_one_stream_only(pkg):
+    """gqa_prefill_get_stream_status waits for its own stream only: a bad-
+    metadata call on a side stream is reported while another stream is still
+    busy with a long kernel, and the read clears the bit."""
+    import time
+    assert pkg.get_device_status() == 0
+    b = W.make_batch([5, 6], [20, 30], 8, 2, 64, "bf16", window=0, sink_mode="none", seed=3)
+    dev = b.to("cuda")
+    bad_kv = dev.kv_indptr.clone()
+    bad_kv[1] += 1
+    out = torch.full_like(dev.q, 7.0)
+    torch.cuda.synchronize()
+    busy, side = torch.cuda.Stream(), torch.cuda.Stream()
+    # load everything the timed part launches (kernels load at first use)
+    with torch.cuda.stream(side):
+        pkg.gqa_flash_prefill(dev.q, dev.k, dev.v, dev.cu_seqlens_q, dev.prefix_lens,
+                              dev.kv_indptr, dev.scale, out=torch.empty_like(dev.q), stream=side)
+    assert pkg.get_stream_status(side) == 0
+    with torch.cuda.stream(busy):
+        torch.cuda._sleep(3_000_000_000)  # about 1.5 s of spinning at 2 GHz
+    with torch.cuda.stream(side):
+        pkg.gqa_flash_prefill(dev.q, dev.k, dev.v, dev.cu_seqlens_q, dev.prefix_lens, bad_kv,
+                              dev.scale, out=out, stream=side)
+    t0 = time.perf_counter()
+    st = pkg.get_stream_status(side)
+    waited = time.perf_counter() - t0
+    assert st == pkg.GQA_DEV_BAD_METADATA
+    assert waited < 0.75, waited  # returned long before the busy stream's kernel ended
+    assert not busy.query()
+    busy.synchronize()
+    assert pkg.get_stream_status(side) == 0  # cleared by the read
+    assert bool((out == 7.0).all())
+
+
+def test_fma_pipe_exp2_against_exp2(pkg):
+    """The softmax's FMA-pipe 2^x (Cody-Waite reduction + fitted degree-3
+    minimax polynomial) against exp2 in fp64 and against the GPU's exp2:
+    relative error at most 7.6e-5 over [-126, 8], exact powers of two at the
+    integers."""
+    x = torch.cat([torch.linspace(-126.0, 8.0, 1_000_003, dtype=torch.float64),
+                   torch.arange(-126, 9, dtype=torch.float64)]).float().cuda()
+    y = pkg.selftest_exp2(x).double()
+    want = torch.exp2(x.double())
+    rel = ((y - want).abs() / want).max().item()
+    assert rel <= 7.6e-5, rel
+    gpu = torch.exp2(x).double()  # the device's own exp2 in fp32
+    assert ((y - gpu).abs() / gpu).max().item() <= 7.7e-5
+    ints = torch.arange(-126, 9, dtype=torch.float32, device="cuda")
+    yi = pkg.selftest_exp2(ints).double()
+    assert ((yi - torch.exp2(ints.double())).abs() / torch.exp2(ints.double())).max() <= 7.6e-5

@@ -49,15 +49,33 @@ def test_noalloc_equals_workspace_entry_over_calls_in_a_row(pkg):
         assert torch.equal(lse, ref_lse), b.name
 
 
+_DECLINE_SCRIPT = r"""
+import ctypes, sys
+sys.path.insert(0, sys.argv[1])
+import gqa_flash_attention_prefill_gb300 as pkg
+lib = pkg.load()
+fake = 1 << 20
+used, nbytes = pkg.splitkv_workspace(1, 4096, 4096, 64, 8, 64, "bf16", 0, 16)
+assert used == 16 and nbytes > pkg.NOALLOC_SCRATCH_BYTES, (used, nbytes)
+rc = lib.gqa_flash_prefill_splitkv_noalloc(fake, fake, fake, fake, fake, fake, 1, 4096, 4096,
+                                           4096, 64, 8, 64, pkg.GQA_BF16, ctypes.c_float(0.125),
+                                           0, None, 0, fake, None, 16, None)
+print("rc", rc)
+"""
+
+
 def test_noalloc_declines_oversize_before_launch(pkg):
     """4096 tokens x 8 KV heads in 16 splits needs ~1 GB of partials: declined
-    (GQA_ERR_UNSUPPORTED) before any device access, so fake addresses are safe."""
-    lib = pkg.load()
-    fake = 1 << 20
-    used, nbytes = pkg.splitkv_workspace(1, 4096, 4096, 64, 8, 64, "bf16", 0, 16)
-    assert used == 16 and nbytes > pkg.NOALLOC_SCRATCH_BYTES
-    rc = lib.gqa_flash_prefill_splitkv_noalloc(fake, fake, fake, fake, fake, fake, 1, 4096, 4096,
-                                               4096, 64, 8, 64, pkg.GQA_BF16,
-                                               ctypes.c_float(0.125), 0, None, 0, fake, None,
-                                               16, None)
-    assert rc == -2
+    (GQA_ERR_UNSUPPORTED) before any device access.  The call passes fake
+    addresses, so it runs in a child process that sees no GPU: were the
+    decline ever to slip, the launch would fail there with GQA_ERR_CUDA
+    instead of touching a device."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", _DECLINE_SCRIPT, root], env=env,
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert "rc -2" in r.stdout, r.stdout
