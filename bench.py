@@ -813,6 +813,7 @@ def run_workload(args, rank, world):
     torch.cuda.set_device(local)
     pkg.load()
     dev = "cuda"
+    masks = None
     if args.workload == "chunked_prefix":
         full = W.chunked_prefix(8, 8192, 8192, 128, seed=2)
         b = W.window_bounded(full, 128) if args.layout == "window-bounded" else full
@@ -847,12 +848,37 @@ def run_workload(args, rank, world):
         desc = ("short chunks over long prefixes: 2 sequences x (prefix 16384 + extend 64), "
                 "64/8, d 64, bf16, sinks; one full-causal and one window-128 call per step")
         tokens = 2 * 128
+    elif args.workload == "tree_verify":
+        # custom mask with and without a sliding window: 8 sequences, 8192
+        # cached tokens each, 64 draft tokens in a random tree per sequence
+        trees = [W.random_tree_mask(64, seed=50 + s_) for s_ in range(8)]
+        full = W.make_batch([8192] * 8, [64] * 8, 64, 8, 64, "bf16", window=0,
+                            sink_mode="head", seed=7, name="tree-verify-full")
+        win = W.window_bounded(W.make_batch([8192] * 8, [64] * 8, 64, 8, 64, "bf16", window=128,
+                                            sink_mode="head", seed=8), 128)
+        calls = [full.to(dev), win.to(dev)]
+        words, indptr = W.pack_custom_mask(trees)
+        masks = [(words.to(dev), indptr.to(dev))] * 2
+        desc = ("custom-mask verify: 8 sequences x (8192 cached + 64 draft tokens in a random "
+                "tree), 64/8, d 64, bf16, sinks; one full-attention and one window-128 "
+                "(window-bounded KV) call per step")
+        tokens = 2 * 8 * 64
     else:
         raise ValueError(args.workload)
     flops = 0.0
-    for b in calls:
-        flops += 4.0 * b.d * b.hq * useful_pairs([int(x) for x in b.prefix_lens.tolist()],
-                                                 b.extend_lens, b.window)
+    for i, b in enumerate(calls):
+        if masks is not None:  # kept pairs under causal, window and custom mask
+            pre = [int(x) for x in b.prefix_lens.tolist()]
+            for s_, (p_, e) in enumerate(zip(pre, b.extend_lens)):
+                for row in range(e):
+                    pos = p_ + row
+                    lo = 0 if b.window <= 0 else max(0, pos - b.window + 1)
+                    n = (min(p_, pos + 1) - min(lo, p_)) + int(
+                        sum(trees[s_][row, j - p_] for j in range(max(lo, p_), pos + 1)))
+                    flops += 4.0 * b.d * b.hq * n
+        else:
+            flops += 4.0 * b.d * b.hq * useful_pairs([int(x) for x in b.prefix_lens.tolist()],
+                                                     b.extend_lens, b.window)
     outs = [torch.empty_like(b.q) for b in calls]
     lses = [torch.empty(b.q.shape[:2], dtype=torch.float32, device=dev) for b in calls]
     stream = torch.cuda.current_stream()
@@ -873,7 +899,9 @@ def run_workload(args, rank, world):
 
     def step():
         for i, (b, o, l) in enumerate(zip(calls, outs, lses)):
-            if args.paged > 0:
+            if masks is not None:
+                pkg.prefill_masked(b, masks[i][0], masks[i][1], out=o, lse=l, stream=stream)
+            elif args.paged > 0:
                 pkg.prefill_paged(paged_calls[i], out=o, lse=l, stream=stream)
             elif args.splits >= 0:
                 pkg.prefill_splitkv(b, num_splits=args.splits, workspace=workspaces[i], out=o,
@@ -926,12 +954,14 @@ def run_workload(args, rank, world):
             "pct_of_bf16_peak": round(100.0 * value / (world * peaks["bf16_tflops"]), 2),
             "gpu_launches": len(calls) * steps + sum(1 for s_ in splits_used if s_ > 1) * steps,
             "clocks": clk.summary()}
-    if args.workload in ("chunked_prefix", "decode"):
+    if masks is not None:
+        line["config"]["entry"] = "gqa_flash_prefill_masked"
+    if args.workload in ("chunked_prefix", "decode", "tree_verify"):
         # HBM-bound: Q read and O (+ lse) written once; of K and V only the rows some
         # window reaches (the window-bounded layout's rows) must be read, in either layout.
         nbytes = 0
         for b in calls:
-            keys = sum(min(p_, b.window) + e for p_, e in
+            keys = sum((min(p_, b.window) if b.window > 0 else p_) + e for p_, e in
                        zip([int(x) for x in b.prefix_lens.tolist()], b.extend_lens))
             nbytes += b.q.numel() * 2 * 2 + keys * b.hkv * b.d * 2 * 2 + b.q.shape[0] * b.hq * 4
         gbs = nbytes / (ms_step * 1e-3) / 1e9
@@ -1064,7 +1094,7 @@ def main():
                     help="--impl reference: total CPU seconds of oracle work over all steps")
     ap.add_argument("--workload", default="oss20b_16k",
                     choices=["oss20b_16k", "layer_pair", "chunked_prefix", "ragged", "ragged_full",
-                             "ragged_grid", "short_chunk", "decode"],
+                             "ragged_grid", "short_chunk", "decode", "tree_verify"],
                     help="oss20b_16k is the headline configuration; the others are "
                          "supplementary measurements")
     ap.add_argument("--layout", default="window-bounded", choices=["window-bounded", "full-prefix"],

@@ -19,7 +19,7 @@ __all__ = ["load", "gqa_flash_prefill", "gqa_flash_prefill_debug", "prefill", "p
            "gqa_flash_prefill_splitkv_noalloc", "prefill_splitkv_noalloc",
            "gqa_flash_prefill_masked", "prefill_masked",
            "NOALLOC_SCRATCH_BYTES", "gqa_flash_prefill_paged", "prefill_paged",
-           "clear_config_cache", "config_block_n", "selftest_timeout", "selftest_exp2", "GQAError",
+           "clear_config_cache", "config_block_n", "selftest_timeout", "GQAError",
            "GQA_F16", "GQA_BF16", "GQA_DEV_TIMEOUT", "GQA_DEV_BAD_METADATA",
            "EXPORTED_SYMBOLS"]
 
@@ -35,7 +35,7 @@ EXPORTED_SYMBOLS = [
     "gqa_prefill_selftest_timeout", "gqa_prefill_force_q_tiles",
     "gqa_flash_prefill_splitkv", "gqa_prefill_splitkv_workspace",
     "gqa_flash_prefill_splitkv_noalloc", "gqa_flash_prefill_paged",
-    "gqa_prefill_get_stream_status", "gqa_flash_prefill_masked", "gqa_prefill_selftest_exp2",
+    "gqa_prefill_get_stream_status", "gqa_flash_prefill_masked",
 ]
 NOALLOC_SCRATCH_BYTES = 32 << 20  # the library's file-scope split-KV scratch (gqa_prefill.h)
 
@@ -101,9 +101,6 @@ def load(path: Optional[str] = None):
     lib.gqa_prefill_get_device_status.restype = ctypes.c_int
     lib.gqa_prefill_get_stream_status.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)]
     lib.gqa_prefill_get_stream_status.restype = ctypes.c_int
-    lib.gqa_prefill_selftest_exp2.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
-                                              ctypes.c_void_p]
-    lib.gqa_prefill_selftest_exp2.restype = ctypes.c_int
     lib.gqa_prefill_status_string.argtypes = [ctypes.c_int]
     lib.gqa_prefill_status_string.restype = ctypes.c_char_p
     lib.gqa_prefill_version.argtypes = []
@@ -464,17 +461,6 @@ def get_stream_status(stream=None) -> int:
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_prefill_get_stream_status")
     return v.value
-
-
-def selftest_exp2(x, stream=None):
-    """2^x through the softmax's FMA-pipe exponential (x: float32 CUDA tensor)."""
-    import torch
-    x = x.contiguous()
-    y = torch.empty_like(x)
-    rc = load().gqa_prefill_selftest_exp2(_ptr(x), _ptr(y), int(x.numel()), _stream_handle(stream))
-    if rc != GQA_OK:
-        raise GQAError(rc, "gqa_prefill_selftest_exp2")
-    return y
 
 
 def get_device_status() -> int:

@@ -31,17 +31,6 @@ __global__ void status_take_kernel(unsigned int* status, unsigned int* snapshot)
   *snapshot = atomicExch(status, 0u);
 }
 
-// Evaluates the softmax's FMA-pipe 2^x (exp2_pair_fma) on n inputs, so that
-// it can be checked against exp2 on the device.
-__global__ void selftest_exp2_kernel(const float* x, float* y, int n) {
-  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
-  if (i >= n) return;
-  float a = x[i], b = (i + 1 < n) ? x[i + 1] : 0.f;
-  exp2_pair_fma(a, b);
-  y[i] = a;
-  if (i + 1 < n) y[i + 1] = b;
-}
-
 // Failure-detection self-test: one thread waits on an mbarrier that nothing
 // ever arrives on, through the same bounded wait the prefill kernel uses.  The
 // wait runs out after `timeout_ns`, raises GQA_DEV_TIMEOUT and the kernel
@@ -961,15 +950,6 @@ int gqa_prefill_selftest_timeout(int timeout_ms, void* stream, int* status) {
   if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return GQA_ERR_CUDA;
   return gqa_prefill_get_device_status(status);
-}
-
-int gqa_prefill_selftest_exp2(const float* x, float* y, int n, void* stream) {
-  if (n < 0 || (n > 0 && (x == nullptr || y == nullptr))) return GQA_ERR_INVALID;
-  if (n == 0) return GQA_OK;
-  const int pairs = (n + 1) / 2;
-  gqa::selftest_exp2_kernel<<<(pairs + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      x, y, n);
-  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
 int gqa_prefill_force_block_n(int block_n) {

@@ -111,18 +111,6 @@ __host__ __device__ constexpr int tmem_alloc_for(int D, int BN, int QT) {
   return QT == 1 ? tmem_cols_for(D, BN) : 512;
 }
 
-// Columns of each 64-column chunk whose exponentials go to the FMA pipe
-// (exp2_pair_fma) on tiles without a mask, for the shapes where the
-// special-function unit's ex2 rate limits the softmax: head dim 64 with
-// 128-key tiles (the full-causal default).  GQA_EMU_COLS overrides it for
-// measurements.
-#ifndef GQA_EMU_COLS
-#define GQA_EMU_COLS 0
-#endif
-__host__ __device__ constexpr int emu_cols(int D, int BN) {
-  return (D == 64 && BN == 128) ? GQA_EMU_COLS : 0;
-}
-
 // Q tiles in flight per CTA: two for d = 64 (the next unit's Q loads during
 // the current unit and two CTAs still fit on an SM), one for larger d.
 __host__ __device__ constexpr int q_buffers(int D) { return D == 64 ? 2 : 1; }
@@ -789,9 +777,6 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
         const bool edge_c = n0 + BN - 1 > U.P + q0s;
         const bool edge_w = WIN && n0 < U.P + qls - win + 1;
         const bool edge_m = MASK && n0 + BN - 1 >= U.P;  // the tile reaches the extend keys
-        // No masked score in the tile: every x below is finite and <= 8.
-        const bool interior = !(edge_c || edge_w || edge_m);
-        constexpr int kEmu = (BN != 96) ? emu_cols(D, BN) : 0;
         n_masked += tile_needs_mask(n0, BN, U.P, U.q0, U.q_last, win) ? 1 : 0;
         // S is processed in CW-column chunks (64, or 48 for 96-key tiles).
         constexpr int CW = (BN == 96) ? 48 : 64;
@@ -884,13 +869,8 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
             for (int t = 0; t < 8; t += 2)
               unf2(ffma2(f2(__uint_as_float(sr[c + t]), __uint_as_float(sr[c + t + 1])), sc2, nm2),
                    x[t], x[t + 1]);
-            if (kEmu > c && interior) {
 #pragma unroll
-              for (int t = 0; t < 8; t += 2) exp2_pair_fma(x[t], x[t + 1]);
-            } else {
-#pragma unroll
-              for (int t = 0; t < 8; ++t) x[t] = ex2(x[t]);
-            }
+            for (int t = 0; t < 8; ++t) x[t] = ex2(x[t]);
             acc0 = fadd2(acc0, f2(x[0], x[1]));
             acc1 = fadd2(acc1, f2(x[2], x[3]));
             acc2 = fadd2(acc2, f2(x[4], x[5]));

@@ -280,37 +280,6 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
   asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-// 2^x for a pair of fp32 values on the FMA and integer pipes, which relieves
-// the special-function unit when exponentials and tensor-core work take
-// equally long (head dim 64).  Cody-Waite range reduction: x = n + f with
-// n = round(x) (adding and subtracting 1.5 * 2^23 rounds to an integer and
-// leaves n in the low mantissa bits), f in [-1/2, 1/2]; 2^f from a degree-3
-// polynomial whose coefficients were fitted here with the Remez exchange
-// algorithm for minimax relative error on [-1/2, 1/2] (7.5e-5, far below
-// the 16-bit rounding the probabilities get next); 2^n enters through an
-// integer add of n << 23 to the polynomial's bit pattern.  Inputs are
-// clamped to [-126, +inf): the callers pass x <= 8.
-constexpr float kExp2Round = 12582912.0f;  // 1.5 * 2^23
-constexpr float kExp2C0 = 0.9999280571937561f;
-constexpr float kExp2C1 = 0.6932609677314758f;
-constexpr float kExp2C2 = 0.2426111251115799f;
-constexpr float kExp2C3 = 0.0551716685295105f;
-__device__ __forceinline__ void exp2_pair_fma(float& a, float& b) {
-  const uint64_t x2 = f2(fmaxf(a, -126.f), fmaxf(b, -126.f));
-  const uint64_t t = fadd2(x2, f2(kExp2Round, kExp2Round));   // 1.5 * 2^23 + round(x)
-  const uint64_t n = fadd2(t, f2(-kExp2Round, -kExp2Round));  // round(x), exact
-  const uint64_t f = ffma2(n, f2(-1.f, -1.f), x2);            // x - round(x)
-  uint64_t q = ffma2(f, f2(kExp2C3, kExp2C3), f2(kExp2C2, kExp2C2));
-  q = ffma2(q, f, f2(kExp2C1, kExp2C1));
-  q = ffma2(q, f, f2(kExp2C0, kExp2C0));
-  float qa, qb, ta, tb;
-  unf2(q, qa, qb);
-  unf2(t, ta, tb);
-  // The low bits of t hold n (two's complement): shifted to the exponent
-  // field, the constant's own bits fall off the top.
-  a = __uint_as_float(__float_as_uint(qa) + (__float_as_uint(ta) << 23));
-  b = __uint_as_float(__float_as_uint(qb) + (__float_as_uint(tb) << 23));
-}
 }  // namespace gqa
 
 namespace gqa {

@@ -291,6 +291,22 @@ def random_custom_mask(extend_lens, density=0.7, seed=0, diagonal=True):
     return out
 
 
+def random_tree_mask(num_tokens, seed=0):
+    """Keep matrix [n, n] of a seeded random draft tree: token t > 0 hangs
+    under a parent drawn uniformly from tokens 0 .. t-1 and keeps exactly its
+    ancestors and itself (the shape of a speculative-decoding verify step)."""
+    import numpy as np
+    rng = np.random.default_rng(int(seed))
+    parent = [-1] + [int(rng.integers(0, t)) for t in range(1, num_tokens)]
+    m = np.zeros((num_tokens, num_tokens), dtype=bool)
+    for t in range(num_tokens):
+        a = t
+        while a >= 0:
+            m[t, a] = True
+            a = parent[a]
+    return m
+
+
 RAGGED_WINDOWS = [1, 15, 64, 127, 128, 129, 4096, 0]
 
 

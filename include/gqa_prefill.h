@@ -384,16 +384,7 @@ GQA_API int gqa_prefill_selftest_timeout(int timeout_ms, void* stream, int* stat
  */
 GQA_API int gqa_prefill_get_device_status(int* status);
 
-/*
- * Self-test of the softmax's 2^x on the FMA pipe (used for a fraction of the
- * exponentials when head dim is 64 and the key tile 128): y[i] = 2^x[i] for
- * n device floats, enqueued on `stream`, for inputs in [-126, 8] (the range
- * the softmax passes: scores minus a running maximum, at most 8 above it).
- * Cody-Waite range reduction and a degree-3 minimax polynomial fitted with
- * the Remez exchange algorithm; relative error at most 7.5e-5 over that
- * range.  Returns GQA_OK, GQA_ERR_INVALID or GQA_ERR_CUDA.
- */
-GQA_API int gqa_prefill_selftest_exp2(const float* x, float* y, int n, void* stream);
+
 
 /*
  * gqa_prefill_get_stream_status -- the same status word, read without a
