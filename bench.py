@@ -559,6 +559,46 @@ def run_oss20b(args, rank, world):
     return line
 
 
+def run_profile(args):
+    """`--profile step`: the warm-up steps and one more step of the 16k
+    prefill (768 calls), untimed, for an ncu launch list or a counter capture
+    of every launch of a step.  `--profile chunk31`: chunk 31's full-causal and
+    window-128 calls once each (the largest calls of the step), for a full
+    ncu capture.  `--profile pair`: the layer pair's two calls once each.
+    Prints nothing but a completion line; no bench values."""
+    import torch
+    import gqa_flash_attention_prefill_gb300 as pkg
+    from gqa_flash_attention_prefill_gb300 import workloads as W
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    pkg.load()
+    stream = torch.cuda.current_stream()
+    if args.profile == "pair":
+        for b in W.layer_pair(seq=4096, seed=1):
+            pkg.prefill(b.to("cuda"), stream=stream)
+        n = 2
+    elif args.profile == "chunk31":
+        st = W.oss20b_stack(num_layers=2, seq=SEQ, chunk_len=CHUNK, seed=3, device="cuda")
+        for layer in (0, 1):
+            pkg.prefill(st.call(SEQ // CHUNK - 1, layer), stream=stream)
+        n = 2
+    else:
+        st, metas, calls = oss20b_setup()
+        out = torch.empty_like(st.q)
+        lse = torch.empty(st.q.shape[:3], dtype=torch.float32, device="cuda")
+        L = CHUNK
+        runs = [pkg.prepare(cl["batch"], out=out[cl["layer"], cl["chunk"] * L:(cl["chunk"] + 1) * L],
+                            lse=lse[cl["layer"], cl["chunk"] * L:(cl["chunk"] + 1) * L],
+                            stream=stream) for cl in calls]
+        for _ in range(args.warmup + 1):
+            for r in runs:
+                r()
+        n = len(runs) * (args.warmup + 1)
+    torch.cuda.synchronize()
+    if pkg.get_device_status() != 0:
+        raise RuntimeError("device status word raised")
+    print(f"profile run done: {n} prefill launches", flush=True)
+
+
 def bench_config(world):
     return {"workload": WORKLOAD, "global_batch": world, "seq_len": SEQ, "chunk_len": CHUNK,
             "layers": LAYERS, "calls_per_step": LAYERS * (SEQ // CHUNK),
@@ -1107,9 +1147,16 @@ def main():
     ap.add_argument("--splits", type=int, default=-1,
                     help="supplementary workloads: -1 the plain entry point; 0 split-KV with "
                          "the library's split count; k >= 1 split-KV with k splits")
+    ap.add_argument("--profile", choices=["step", "chunk31", "pair"], default=None,
+                    help="untimed run for an ncu capture: the warm-up steps plus one step of "
+                         "the 16k prefill, chunk 31's two calls, or the layer pair's two "
+                         "calls; prints no bench line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.profile is not None:
+        run_profile(args)
+        return
     rank, world = dist_setup()
     if args.impl == "reference":
         line = run_reference(args, rank, world)
