@@ -34,7 +34,7 @@
 namespace gqa {
 
 constexpr int kMaxSeqs = 512;        // sequences per launch (shared-memory tables)
-constexpr int kSortSeqs = 64;        // launches with at most this many sequences deal them costliest first
+static_assert((kMaxSeqs & (kMaxSeqs - 1)) == 0, "the dealing-order sort packs indices below kMaxSeqs");
 // Threads per CTA with QT query tiles: a softmax warpgroup per tile, one
 // producer warp and one MMA warp.
 __host__ __device__ constexpr int threads_for(int QT) { return 32 * (4 * QT + 2); }
@@ -335,6 +335,64 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity,
 }
 
 
+// Dealing order of a batch's sequences, costliest first: keys[b] holds
+// sequence b's costliest-unit tile count (-1: no units) and order[r]
+// receives the sequence dealt r-th.  Sequences are sorted by decreasing key,
+// ties by index, so the long units of every sequence go out before any
+// short one (inside a sequence the units are already dealt costliest
+// first).  A batch whose keys all lie within a factor of two (a windowed
+// decode step) keeps its order: there the deal order does not matter.  The
+// sort is a bitonic sort, descending, of the composites key * 512 +
+// (511 - index) (keys clamped to 2^22 - 1; the padding up to a power of two
+// holds -1 and sorts last).  Called by every thread of the CTA; `scratch`
+// is two shared words.  Kept out of line, so that the kernel body, and with
+// it the placement of its hot loops, does not depend on it.
+static __device__ __noinline__ void deal_order(const int32_t* keys, int32_t* order, int32_t* scratch,
+                                        int nseq, int tid, int nthreads) {
+  if (tid == 0) {
+    scratch[0] = 0x7fffffff;
+    scratch[1] = -1;
+  }
+  __syncthreads();
+  int kmin = 0x7fffffff, kmax = -1;
+  for (int b = tid; b < nseq; b += nthreads) {
+    const int k = keys[b];
+    if (k >= 0) {
+      kmin = min(kmin, k);
+      kmax = max(kmax, k);
+    }
+  }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if ((tid & 31) == 0) {
+    atomicMin(&scratch[0], kmin);
+    atomicMax(&scratch[1], kmax);
+  }
+  __syncthreads();
+  if (scratch[1] < 2 * max(scratch[0], 1)) return;  // uniform: every thread reads the same words
+  int n = 2;
+  while (n < nseq) n <<= 1;
+  for (int i = tid; i < n; i += nthreads)
+    order[i] = i < nseq ? min(max(keys[i], 0), (1 << 22) - 1) * kMaxSeqs + (kMaxSeqs - 1 - i) : -1;
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      __syncthreads();
+      for (int i = tid; i < n / 2; i += nthreads) {
+        const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
+        const bool desc = (lo & size) == 0;  // direction of this bitonic run
+        const int x = order[lo], y = order[hi];
+        if ((x < y) == desc) {
+          order[lo] = y;
+          order[hi] = x;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  for (int r = tid; r < nseq; r += nthreads) order[r] = kMaxSeqs - 1 - (order[r] & (kMaxSeqs - 1));
+  __syncthreads();
+}
+
 // SPL: split-KV work items writing partials; PAGED: K/V from a page pool;
 // MASK: the custom mask ANDed into the causal / window mask.  Each is a
 // separate instantiation, so the default kernel carries none of their code.
@@ -453,31 +511,9 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
   }
   if (bad) misc[2] = 1u;
   __syncthreads();
-  // Costliest first across the batch: a small batch deals its sequences by
-  // decreasing key (ties by index), so the long units of every sequence go
-  // out before any short one; inside a sequence the units are already dealt
-  // costliest first.  Larger batches keep their own order (the ranking costs
-  // batch-size squared comparisons).
-  if (nseq > 1 && nseq <= kSortSeqs) {
-    int rank[(kSortSeqs + kThr - 1) / kThr];
-#pragma unroll
-    for (int i = 0; i < (kSortSeqs + kThr - 1) / kThr; ++i) {
-      const int b = b_lo + i;
-      rank[i] = 0;
-      if (b < b_hi) {
-        const int kb = tile_start[b];
-        for (int o = 0; o < nseq; ++o) {
-          const int ko = tile_start[o];
-          rank[i] += (ko > kb || (ko == kb && o < b)) ? 1 : 0;
-        }
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < (kSortSeqs + kThr - 1) / kThr; ++i)
-      if (b_lo + i < b_hi) seq_order[rank[i]] = b_lo + i;
-    __syncthreads();
-  }
+  // Costliest sequences first (deal_order); one call whatever the batch, so
+  // the kernel body stays the same size.
+  if (nseq > 1) deal_order(tile_start, seq_order, scan + 14, nseq, tid, kThr);
   // Units per sequence in dealing order, then their exclusive scan: warp
   // scans, then warp totals.  tile_start[r] is the first unit (of one KV
   // head) of the r-th sequence dealt.

@@ -462,13 +462,24 @@ def test_splitkv_and_paged_over_600_sequences(pkg):
     compare(out.cpu(), lse.cpu(), ref, ref_lse, label="paged, 600 sequences")
 
 
-def test_units_dealt_costliest_first_across_the_batch(pkg):
+def _decode_batch_300():
+    gen = torch.Generator().manual_seed(300)
+    pre = torch.randint(0, 6000, (300,), generator=gen).tolist()
+    return W.make_batch(pre, [1] * 300, 16, 2, 64, "bf16", window=0, sink_mode="head", seed=300)
+
+
+@pytest.mark.parametrize("which", ["ragged6", "decode300"])
+def test_units_dealt_costliest_first_across_the_batch(pkg, which):
     """The unit records' (CTA, position) give each unit's place in the deal;
     in that order the sequences come by decreasing cost of their costliest
     unit (ties by index), each sequence's units by decreasing query position,
-    and every unit appears once."""
-    b = W.make_batch([0, 37, 5000, 129, 64, 3000], [1, 300, 700, 128, 129, 2000], 64, 8, 64,
-                     "bf16", window=0, sink_mode="head", seed=77)
+    and every unit appears once: a 6-sequence ragged prefill and a
+    300-sequence decode step with prefixes U[0, 6000)."""
+    if which == "ragged6":
+        b = W.make_batch([0, 37, 5000, 129, 64, 3000], [1, 300, 700, 128, 129, 2000], 64, 8, 64,
+                         "bf16", window=0, sink_mode="head", seed=77)
+    else:
+        b = _decode_batch_300()
     p, used = _bookkeeping(pkg, b)
     grid = p["grid"]
     cta, k = used[:, 6].astype(np.int64), used[:, 7].astype(np.int64)
