@@ -881,6 +881,13 @@ def run_workload(args, rank, world):
         desc = (f"windowed decode: 128 sequences x 1 new token over prefixes U[1024,16384], "
                 f"64/8, d 64, bf16, window 128, sinks, {args.layout} KV layout")
         tokens = 128
+    elif args.workload == "decode_full":
+        b = W.decode(num_seqs=256, min_prefix=1024, max_prefix=16384, window=0,
+                     sink_mode="head", seed=6)
+        calls = [b.to(dev)]
+        desc = ("full-attention decode: 256 sequences x 1 new token over prefixes "
+                "U[1024,16384], 64/8, d 64, bf16, sinks (every prefix key read once)")
+        tokens = 256
     elif args.workload == "short_chunk":
         calls = [W.make_batch([16384, 16384], [64, 64], 64, 8, 64, "bf16", window=w,
                               sink_mode="head", seed=5 + i, name=f"short-chunk-w{w}").to(dev)
@@ -996,7 +1003,7 @@ def run_workload(args, rank, world):
             "clocks": clk.summary()}
     if masks is not None:
         line["config"]["entry"] = "gqa_flash_prefill_masked"
-    if args.workload in ("chunked_prefix", "decode", "tree_verify"):
+    if args.workload in ("chunked_prefix", "decode", "decode_full", "tree_verify"):
         # HBM-bound: Q read and O (+ lse) written once; of K and V only the rows some
         # window reaches (the window-bounded layout's rows) must be read, in either layout.
         nbytes = 0
@@ -1134,7 +1141,8 @@ def main():
                     help="--impl reference: total CPU seconds of oracle work over all steps")
     ap.add_argument("--workload", default="oss20b_16k",
                     choices=["oss20b_16k", "layer_pair", "chunked_prefix", "ragged", "ragged_full",
-                             "ragged_grid", "short_chunk", "decode", "tree_verify"],
+                             "ragged_grid", "short_chunk", "decode", "decode_full",
+                             "tree_verify"],
                     help="oss20b_16k is the headline configuration; the others are "
                          "supplementary measurements")
     ap.add_argument("--layout", default="window-bounded", choices=["window-bounded", "full-prefix"],
