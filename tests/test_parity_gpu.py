@@ -499,3 +499,26 @@ def test_units_dealt_costliest_first_across_the_batch(pkg, which):
     for s in order:
         q0 = rec[rec[:, 0] == s][:, 2]
         assert np.all(np.diff(q0) <= 0)  # KV heads fastest, positions decreasing
+
+
+# ------------------------------------------------------------- large sizes
+
+def test_long_single_sequence_sampled(pkg):
+    """One 32768-token prefill (16384 units at G = 8), full causal: the last
+    rows see 32768 keys; sampled rows against the oracle."""
+    b = W.make_batch([0], [32768], 64, 8, 64, "bf16", window=0, sink_mode="head", seed=32768,
+                     name="single-32k")
+    rows = np.array([0, 1, 127, 128, 4095, 16383, 16384, 30000, 32766, 32767], dtype=np.int64)
+    _check_sampled(pkg, b, rows)
+
+
+def test_window_over_a_256k_prefix(pkg):
+    """A 512-token chunk over a 262144-token cached prefix, window 128, the
+    whole prefix handed over: the kernel's loop floor skips to the window;
+    checked against the oracle on the window-bounded layout (the same result,
+    an oracle pin), every row."""
+    full = W.make_batch([262144], [512], 64, 8, 64, "bf16", window=128, sink_mode="head",
+                        seed=262144, name="chunk-over-256k")
+    out, lse = run_gpu(pkg, full)
+    ref, ref_lse = run_oracle(W.window_bounded(full, 128))
+    compare(out, lse, ref, ref_lse, label=full.name)
