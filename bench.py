@@ -425,6 +425,27 @@ def oss20b_setup(device="cuda", num_layers=LAYERS, seq=SEQ, chunk=CHUNK):
     return st, metas, calls
 
 
+def step_workspace(pkg, mode):
+    """The one workspace the 16k step's balanced-split calls share (they run
+    in stream order), or None when `mode` is "none"."""
+    import torch
+    if mode == "none":
+        return None
+    nbytes = max(pkg.splitkv_workspace(1, CHUNK, CHUNK, 64, 8, 64, "bf16", w,
+                                       pkg.SPLITS_BALANCED)[1] for w in (0, 128))
+    return torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+
+
+def step_prepare(pkg, batch, kind, mode, ws, out, lse, stream):
+    """A prepared call of the 16k step: the plain entry point, or the
+    balanced split for the full-causal calls (`mode` "full") or all calls
+    ("all")."""
+    bal = mode == "all" or (mode == "full" and kind == "full_causal")
+    return pkg.prepare(batch, out=out, lse=lse, stream=stream,
+                       num_splits=pkg.SPLITS_BALANCED if bal else None,
+                       workspace=ws if bal else None)
+
+
 def run_oss20b(args, rank, world):
     """Headline: the 16k chunked prefill, 768 calls per step."""
     import torch
@@ -438,10 +459,12 @@ def run_oss20b(args, rank, world):
     lse = torch.empty(st.q.shape[:3], dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
     L = CHUNK
+    ws = step_workspace(pkg, args.balanced)
     for cl in calls:
         c, layer = cl["chunk"], cl["layer"]
-        cl["run"] = pkg.prepare(cl["batch"], out=out[layer, c * L:(c + 1) * L],
-                                lse=lse[layer, c * L:(c + 1) * L], stream=stream)
+        cl["run"] = step_prepare(pkg, cl["batch"], cl["kind"], args.balanced, ws,
+                                 out[layer, c * L:(c + 1) * L], lse[layer, c * L:(c + 1) * L],
+                                 stream)
     flops = sum(cl["flops"] for cl in calls)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
 
@@ -514,7 +537,7 @@ def run_oss20b(args, rank, world):
     value = world * flops / (ms_step * 1e-3) / 1e12
     full_tf = kind_flops["full_causal"] / (kind_ms["full_causal"] * 1e-3) / 1e12
     win_gbs = win_bytes / (kind_ms["window_128"] * 1e-3) / 1e9
-    e2e = oss20b_e2e(args, st, metas, calls, out, lse, stream, world, flops)
+    e2e = oss20b_e2e(args, st, metas, calls, out, lse, stream, world, flops, ws)
     del flush
     pair = layer_pair_summary(args, world, peaks)
 
@@ -523,7 +546,7 @@ def run_oss20b(args, rank, world):
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) Q/K/V and sinks; no model weights)",
-        "config": bench_config(world),
+        "config": bench_config(world, args.balanced),
         "ms_per_step_mean": round(ms_mean, 4),
         "tokens_per_s": round(world * SEQ / (ms_step * 1e-3), 1),
         "pct_of_bf16_peak": round(100.0 * value / (world * peaks["bf16_tflops"]), 2),
@@ -578,17 +601,23 @@ def run_profile(args):
         n = 2
     elif args.profile == "chunk31":
         st = W.oss20b_stack(num_layers=2, seq=SEQ, chunk_len=CHUNK, seed=3, device="cuda")
+        ws = step_workspace(pkg, args.balanced)
         for layer in (0, 1):
-            pkg.prefill(st.call(SEQ // CHUNK - 1, layer), stream=stream)
+            b = st.call(SEQ // CHUNK - 1, layer)
+            kind = "window_128" if b.window > 0 else "full_causal"
+            step_prepare(pkg, b, kind, args.balanced, ws, torch.empty_like(b.q),
+                         torch.empty(b.q.shape[:2], dtype=torch.float32, device="cuda"), stream)()
         n = 2
     else:
         st, metas, calls = oss20b_setup()
         out = torch.empty_like(st.q)
         lse = torch.empty(st.q.shape[:3], dtype=torch.float32, device="cuda")
         L = CHUNK
-        runs = [pkg.prepare(cl["batch"], out=out[cl["layer"], cl["chunk"] * L:(cl["chunk"] + 1) * L],
-                            lse=lse[cl["layer"], cl["chunk"] * L:(cl["chunk"] + 1) * L],
-                            stream=stream) for cl in calls]
+        ws = step_workspace(pkg, args.balanced)
+        runs = [step_prepare(pkg, cl["batch"], cl["kind"], args.balanced, ws,
+                             out[cl["layer"], cl["chunk"] * L:(cl["chunk"] + 1) * L],
+                             lse[cl["layer"], cl["chunk"] * L:(cl["chunk"] + 1) * L], stream)
+                for cl in calls]
         for _ in range(args.warmup + 1):
             for r in runs:
                 r()
@@ -599,15 +628,19 @@ def run_profile(args):
     print(f"profile run done: {n} prefill launches", flush=True)
 
 
-def bench_config(world):
+def bench_config(world, balanced="none"):
+    entry = {"none": "gqa_flash_prefill",
+             "full": "gqa_flash_prefill_splitkv (balanced split) for the full-causal calls, "
+                     "gqa_flash_prefill for the window-128 calls",
+             "all": "gqa_flash_prefill_splitkv (balanced split)"}[balanced]
     return {"workload": WORKLOAD, "global_batch": world, "seq_len": SEQ, "chunk_len": CHUNK,
             "layers": LAYERS, "calls_per_step": LAYERS * (SEQ // CHUNK),
             "l2": "inputs larger than L2 (3.8 GB read per step); 256 MiB written between steps",
             "parallelism": "replicas (one per GPU)" if world > 1 else "single GPU",
-            "entry": "gqa_flash_prefill"}
+            "entry": entry}
 
 
-def oss20b_e2e(args, st, metas, calls, out, lse, stream, world, flops):
+def oss20b_e2e(args, st, metas, calls, out, lse, stream, world, flops, ws=None):
     """The 16k prefill end to end through the C ABI from pinned host memory:
     every step uploads each chunk's Q rows, its new K and V rows and its
     metadata for all 24 layers, runs the chunk's 24 calls, and downloads the
@@ -641,8 +674,10 @@ def oss20b_e2e(args, st, metas, calls, out, lse, stream, world, flops):
     out2, lse2 = torch.empty_like(out), torch.empty_like(lse)
     sets = []
     for s_, m_, o_, l_ in ((st, metas, out, lse), (st2, metas2, out2, lse2)):
-        runs = [[pkg.prepare(s_.call(c, layer, m_[c]), out=o_[layer, c * L:(c + 1) * L],
-                             lse=l_[layer, c * L:(c + 1) * L], stream=stream)
+        runs = [[step_prepare(pkg, s_.call(c, layer, m_[c]),
+                              "window_128" if s_.windows[layer] > 0 else "full_causal",
+                              args.balanced, ws, o_[layer, c * L:(c + 1) * L],
+                              l_[layer, c * L:(c + 1) * L], stream)
                  for layer in range(n_l)] for c in range(n_c)]
         sets.append({"st": s_, "metas": m_, "out": o_, "lse": l_, "runs": runs,
                      "in_ready": [torch.cuda.Event() for _ in range(n_c)],
@@ -1120,7 +1155,7 @@ def run_reference(args, rank, world):
             "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) Q/K/V and sinks; no model weights)",
-            "config": bench_config(world),
+            "config": bench_config(world, args.balanced),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -1155,6 +1190,9 @@ def main():
     ap.add_argument("--splits", type=int, default=-1,
                     help="supplementary workloads: -1 the plain entry point; 0 split-KV with "
                          "the library's split count; k >= 1 split-KV with k splits")
+    ap.add_argument("--balanced", choices=["none", "full", "all"], default="none",
+                    help="16k prefill: the balanced split (gqa_flash_prefill_splitkv with "
+                         "GQA_SPLITS_BALANCED) for no call, the full-causal calls, or all calls")
     ap.add_argument("--profile", choices=["step", "chunk31", "pair"], default=None,
                     help="untimed run for an ncu capture: the warm-up steps plus one step of "
                          "the 16k prefill, chunk 31's two calls, or the layer pair's two "

@@ -20,12 +20,13 @@ __all__ = ["load", "gqa_flash_prefill", "gqa_flash_prefill_debug", "prefill", "p
            "gqa_flash_prefill_masked", "prefill_masked",
            "NOALLOC_SCRATCH_BYTES", "gqa_flash_prefill_paged", "prefill_paged",
            "clear_config_cache", "config_block_n", "selftest_timeout", "GQAError",
-           "GQA_F16", "GQA_BF16", "GQA_DEV_TIMEOUT", "GQA_DEV_BAD_METADATA",
+           "GQA_F16", "GQA_BF16", "GQA_DEV_TIMEOUT", "GQA_DEV_BAD_METADATA", "SPLITS_BALANCED",
            "EXPORTED_SYMBOLS"]
 
 GQA_F16, GQA_BF16 = 0, 1
 GQA_OK, GQA_ERR_INVALID, GQA_ERR_UNSUPPORTED, GQA_ERR_CUDA = 0, -1, -2, -3
 GQA_DEV_TIMEOUT, GQA_DEV_BAD_METADATA = 1, 2
+SPLITS_BALANCED = -1  # num_splits of the balanced split (GQA_SPLITS_BALANCED)
 
 EXPORTED_SYMBOLS = [
     "gqa_flash_prefill", "gqa_flash_prefill_debug", "gqa_prefill_plan",
@@ -367,31 +368,38 @@ def prefill(batch, out=None, lse=None, with_lse=True, stream=None):
 
 
 class PreparedCall:
-    """gqa_flash_prefill with its arguments marshalled once: calling the
-    object re-issues the same C ABI call (same buffers, same stream), which
-    keeps the host cost of a call to the ctypes round trip.  For callers that
+    """gqa_flash_prefill (or, with ``num_splits``, gqa_flash_prefill_splitkv
+    on ``workspace``) with its arguments marshalled once: calling the object
+    re-issues the same C ABI call (same buffers, same stream), which keeps
+    the host cost of a call to the ctypes round trip.  For callers that
     replay a fixed sequence of calls over resident buffers, such as the
     layers of a prefill."""
 
-    __slots__ = ("_fn", "_args", "out", "lse")
+    __slots__ = ("_fn", "_args", "_name", "out", "lse", "workspace")
 
-    def __init__(self, batch, out, lse=None, stream=None):
-        self._fn = load().gqa_flash_prefill
-        self._args = _args(batch.q, batch.k, batch.v, batch.cu_seqlens_q, batch.prefix_lens,
-                           batch.kv_indptr, batch.scale, batch.window, batch.sinks,
-                           batch.smooth, out, lse, stream, batch.max_seqlen_q)
-        self.out, self.lse = out, lse
+    def __init__(self, batch, out, lse=None, stream=None, num_splits=None, workspace=None):
+        a = _args(batch.q, batch.k, batch.v, batch.cu_seqlens_q, batch.prefix_lens,
+                  batch.kv_indptr, batch.scale, batch.window, batch.sinks, batch.smooth, out, lse,
+                  stream, batch.max_seqlen_q)
+        if num_splits is None:
+            self._fn, self._name, self._args = load().gqa_flash_prefill, "gqa_flash_prefill", a
+        else:
+            nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+            self._fn, self._name = load().gqa_flash_prefill_splitkv, "gqa_flash_prefill_splitkv"
+            self._args = a[:-1] + (int(num_splits), _ptr(workspace), nbytes, a[-1])
+        self.out, self.lse, self.workspace = out, lse, workspace
 
     def __call__(self):
         rc = self._fn(*self._args)
         if rc != GQA_OK:
-            raise GQAError(rc, "gqa_flash_prefill")
+            raise GQAError(rc, self._name)
 
 
-def prepare(batch, out, lse=None, stream=None) -> PreparedCall:
+def prepare(batch, out, lse=None, stream=None, num_splits=None, workspace=None) -> PreparedCall:
     """A PreparedCall of one ``workloads.Batch`` already on the GPU, writing
-    ``out`` (and ``lse`` when given) on ``stream``."""
-    return PreparedCall(batch, out, lse, stream)
+    ``out`` (and ``lse`` when given) on ``stream``; with ``num_splits`` (for
+    example SPLITS_BALANCED) the split-KV entry point on ``workspace``."""
+    return PreparedCall(batch, out, lse, stream, num_splits, workspace)
 
 
 def plan(num_seqs, total_q, max_seqlen_q, hq, hkv, d, dtype, window) -> dict:

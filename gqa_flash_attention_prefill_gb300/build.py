@@ -19,7 +19,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgqa_prefill.so")
 SOURCES = ["host.cu", "inst_d64.cu", "inst_d64_pair.cu", "inst_d128.cu", "inst_d256.cu",
-           "inst_split.cu", "inst_paged.cu", "inst_mask.cu", "merge.cu", "noalloc.cu"]
+           "inst_split.cu", "inst_paged.cu", "inst_mask.cu", "inst_balanced.cu", "merge.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

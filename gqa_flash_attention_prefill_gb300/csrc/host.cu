@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -210,8 +211,11 @@ struct SplitArgs {
   float* part_o = nullptr;
   float* part_ml = nullptr;
   int32_t* part_hdr = nullptr;
+  bool balanced = false;  // balanced split: one kernel, cut units merged in it
+  unsigned long long* sk_count = nullptr;
 };
 constexpr int kMaxSplits = 16;
+constexpr int kBalanced = -1;  // num_splits value requesting the balanced split
 
 // Paged KV: the page table and the pool geometry (indices == nullptr: the
 // contiguous layout).
@@ -243,6 +247,36 @@ SplitLayout split_layout(const Plan& pl, int d, int S) {
   L.hdr_off = L.ml_off + al(items * rows * 8u);
   L.bytes = L.hdr_off + al((4u + 4u * (size_t)pl.max_units) * 4u);
   return L;
+}
+
+// Workspace layout of the balanced split: two partial slots per resident CTA
+// (O in fp32 and (m, l) per row of its first and its last piece), and four
+// count words per unit, each 256-byte aligned.
+struct BalancedLayout {
+  size_t o_off, ml_off, cnt_off, bytes;
+};
+BalancedLayout balanced_layout(const Plan& pl, int d) {
+  auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t slots = 2u * (size_t)pl.slots;
+  BalancedLayout L;
+  L.o_off = 0;
+  L.ml_off = al(slots * 128u * (size_t)d * 4u);
+  L.cnt_off = L.ml_off + al(slots * 128u * 8u);
+  L.bytes = L.cnt_off + al((size_t)pl.max_units * 4u * 8u);
+  return L;
+}
+
+// Launch epochs of the balanced split's count words: unique within the
+// process (48 bits), from a per-process starting point so that words left in
+// reused memory by another process are not taken for this one's.
+unsigned long long next_epoch() {
+  static std::atomic<unsigned long long> next{[] {
+    unsigned long long x = (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count();
+    static int anchor = 0;
+    x ^= (unsigned long long)reinterpret_cast<uintptr_t>(&anchor) * 0x9E3779B97F4A7C15ull;
+    return x;
+  }()};
+  return next.fetch_add(1ull, std::memory_order_relaxed) & ((1ull << 48) - 1ull);
 }
 
 // Split count when the caller leaves it to the library: only when the units
@@ -459,11 +493,14 @@ int launch_planned(const Plan& pl, const void* q, const void* k, const void* v,
   p.part_o = sp.part_o;
   p.part_ml = sp.part_ml;
   p.part_hdr = sp.part_hdr;
+  p.sk_count = sp.sk_count;
+  p.epoch = sp.balanced ? next_epoch() : 0ull;
   int grid = pl.grid;
   if (p.num_splits > 1) {  // more work items than units: fill the resident slots
     const long long items = (long long)pl.max_units * p.num_splits;
     grid = (int)(items < pl.slots ? items : pl.slots);
   }
+  if (sp.balanced) grid = pl.slots;  // one share per resident CTA
   const bool win = p.window > 0;
   const bool bf16 = dtype == GQA_BF16;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -472,6 +509,8 @@ int launch_planned(const Plan& pl, const void* q, const void* k, const void* v,
     e = launch_mask(p, pl.shape, d, win, bf16, grid, pl.smem_launch, st);
   else if (paged)
     e = launch_paged(p, pl.shape, d, win, bf16, grid, pl.smem_launch, st);
+  else if (sp.balanced)
+    e = launch_balanced(p, pl.shape, d, win, bf16, grid, pl.smem_launch, st);
   else if (p.num_splits > 1)
     e = launch_split(p, pl.shape, d, win, bf16, grid, pl.smem_launch, st);
   else if (d == 64)
@@ -485,10 +524,11 @@ int launch_planned(const Plan& pl, const void* q, const void* k, const void* v,
   if (debug_flag())
     std::fprintf(stderr,
                  "[gqa_prefill] B=%d total_q=%d total_kv=%d Hq=%d Hkv=%d d=%d %s window=%d "
-                 "sink=%s block_n=%d q_tiles=%d stages=%d grid=%d (%d/SM) max_units=%d -> %s\n",
+                 "sink=%s block_n=%d q_tiles=%d stages=%d grid=%d (%d/SM) max_units=%d%s -> %s\n",
                  num_seqs, total_q, total_kv, Hq, Hkv, d, bf16 ? "bf16" : "f16", p.window,
                  sinks ? "head" : (p.smooth ? "smooth" : "none"), pl.shape.block_n,
                  pl.shape.q_tiles, pl.shape.kv_stages, grid, pl.ctas_per_sm, pl.max_units,
+                 sp.balanced ? " balanced" : "",
                  e == cudaSuccess ? "launched" : cudaGetErrorString(e));
   return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
@@ -623,13 +663,34 @@ int plan_split(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, int
   return GQA_OK;
 }
 
+// The plan of a balanced-split call: as plan_split's, and declined when one
+// launch's query tiles could overflow the shared-memory scratch the kernel
+// computes the shares in (its K/V rings, one word per query tile plus one).
+int plan_balanced(int num_seqs, int total_q, int max_seqlen_q, int Hq, int Hkv, int d, int dtype,
+                  int window, Plan* pl) {
+  int rc = make_plan(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, pl);
+  if (rc != GQA_OK) return rc;
+  if (!split_shape(d, pl->shape.block_n, pl->shape.q_tiles)) {
+    const int bn = split_shape(d, pl->shape.block_n, 1) ? pl->shape.block_n : (d == 64 ? 128 : 64);
+    rc = make_plan_bn(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, bn, 1, pl);
+    if (rc != GQA_OK) return rc;
+  }
+  const long long seqs = num_seqs < kMaxSeqs ? num_seqs : kMaxSeqs;
+  const long long qtiles = (total_q + pl->unit_rows - 1) / pl->unit_rows + seqs;
+  const long long ring_words = 2ll * pl->shape.kv_stages * pl->shape.block_n * d * 2 / 4;
+  if (qtiles + 1 > ring_words) return GQA_ERR_UNSUPPORTED;
+  // The kernel's share arithmetic is 32-bit for grids below 46341 CTAs.
+  if (pl->slots >= 46341) return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+
 int run(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
         const int32_t* prefix_lens, const int32_t* kv_indptr, int num_seqs, int total_q,
         int total_kv, int max_seqlen_q, int Hq, int Hkv, int d, int dtype, float scale,
         int window, const float* sinks, int smooth_softmax, void* out, float* lse, void* stream,
         int32_t* unit_log, int num_splits = 1, void* workspace = nullptr,
         size_t workspace_bytes = 0, ScratchFn scratch = nullptr) {
-  if (num_splits < 0 || num_splits > kMaxSplits) return GQA_ERR_INVALID;
+  if (num_splits < kBalanced || num_splits > kMaxSplits) return GQA_ERR_INVALID;
   if (num_seqs < 0 || total_q < 0 || total_kv < 0 || max_seqlen_q < 0) return GQA_ERR_INVALID;
   if (Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return GQA_ERR_INVALID;
   if (dtype != GQA_F16 && dtype != GQA_BF16) return GQA_ERR_INVALID;
@@ -660,12 +721,33 @@ int run(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q
   }
   Plan pl;
   SplitArgs sp;
-  const int rc = (num_splits == 1)
-                     ? make_plan(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, &pl)
-                     : plan_split(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window,
-                                  num_splits, &pl, &sp.num_splits);
+  const int rc =
+      (num_splits == 1)
+          ? make_plan(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, &pl)
+      : (num_splits == kBalanced)
+          ? plan_balanced(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, &pl)
+          : plan_split(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window, num_splits,
+                       &pl, &sp.num_splits);
   if (rc != GQA_OK) return rc;
-  if (sp.num_splits > 1) {
+  if (num_splits == kBalanced) {
+    // The kernel counts key tiles in 32 bits: a unit walks at most
+    // ceil(total_kv / block_n) + 1 tiles.
+    const long long unit_tiles = (total_kv + pl.shape.block_n - 1) / pl.shape.block_n + 1;
+    if ((long long)pl.max_units * unit_tiles >= (1ll << 31)) return GQA_ERR_UNSUPPORTED;
+    const BalancedLayout L = balanced_layout(pl, d);
+    if (workspace == nullptr && scratch != nullptr) {
+      const int rs = scratch(L.bytes, &workspace, &workspace_bytes);
+      if (rs != GQA_OK) return rs;
+    }
+    if (workspace == nullptr || workspace_bytes < L.bytes ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+      return GQA_ERR_INVALID;
+    char* base = static_cast<char*>(workspace);
+    sp.balanced = true;
+    sp.part_o = reinterpret_cast<float*>(base + L.o_off);
+    sp.part_ml = reinterpret_cast<float*>(base + L.ml_off);
+    sp.sk_count = reinterpret_cast<unsigned long long*>(base + L.cnt_off);
+  } else if (sp.num_splits > 1) {
     const SplitLayout L = split_layout(pl, d, sp.num_splits);
     if (workspace == nullptr && scratch != nullptr) {
       // The library's own scratch, checked against this very plan's layout.
@@ -880,8 +962,16 @@ int gqa_prefill_splitkv_workspace(int num_seqs, int total_q, int max_seqlen_q, i
                                   int d, int dtype, int window, int num_splits, int* splits_used,
                                   size_t* bytes) {
   if (splits_used == nullptr || bytes == nullptr) return GQA_ERR_INVALID;
-  if (num_splits < 0 || num_splits > gqa::kMaxSplits) return GQA_ERR_INVALID;
+  if (num_splits < gqa::kBalanced || num_splits > gqa::kMaxSplits) return GQA_ERR_INVALID;
   gqa::Plan pl;
+  if (num_splits == gqa::kBalanced) {
+    const int rb = gqa::plan_balanced(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window,
+                                      &pl);
+    if (rb != GQA_OK) return rb;
+    *splits_used = gqa::kBalanced;
+    *bytes = gqa::balanced_layout(pl, d).bytes;
+    return GQA_OK;
+  }
   int S = 1;
   const int rc = gqa::plan_split(num_seqs, total_q, max_seqlen_q, Hq, Hkv, d, dtype, window,
                                  num_splits, &pl, &S);

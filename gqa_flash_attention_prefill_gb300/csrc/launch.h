@@ -48,6 +48,10 @@ cudaError_t launch_paged(const PrefillParams& p, const KernelShape& ks, int d, b
 cudaError_t launch_mask(const PrefillParams& p, const KernelShape& ks, int d, bool win,
                         bool bf16, int grid, unsigned smem, cudaStream_t st);
 
+// Balanced-split instantiations (inst_balanced.cu), same shapes as split_shape.
+cudaError_t launch_balanced(const PrefillParams& p, const KernelShape& ks, int d, bool win,
+                            bool bf16, int grid, unsigned smem, cudaStream_t st);
+
 // Split-KV merge (merge.cu): one 128-thread block per unit, `grid` >= units.
 cudaError_t launch_merge(const PrefillParams& p, int d, bool bf16, int part_rows, int grid,
                          cudaStream_t st);
@@ -107,9 +111,9 @@ struct SmemAttr {
 };
 
 template <int D, int BN, int NS, bool WIN, bool BF16, int MINB, int QT, bool SPL, bool PAGED,
-          bool MASK = false>
+          bool MASK = false, bool SK = false>
 cudaError_t launch_one(const PrefillParams& p, int grid, unsigned smem, cudaStream_t st) {
-  auto kern = prefill_kernel<D, BN, NS, WIN, BF16, MINB, QT, SPL, PAGED, MASK>;
+  auto kern = prefill_kernel<D, BN, NS, WIN, BF16, MINB, QT, SPL, PAGED, MASK, SK>;
   static SmemAttr attr{};
   if (smem < smem_bytes_for(D, BN, NS, QT)) return cudaErrorInvalidValue;
   int dev = 0;
@@ -125,14 +129,14 @@ cudaError_t launch_one(const PrefillParams& p, int grid, unsigned smem, cudaStre
 }
 
 template <int D, int BN, int NS, int MINB, int QT, bool SPL = false, bool PAGED = false,
-          bool MASK = false>
+          bool MASK = false, bool SK = false>
 cudaError_t launch_variants(const PrefillParams& p, bool win, bool bf16, int grid, unsigned smem,
                             cudaStream_t st) {
   if (win)
-    return bf16 ? launch_one<D, BN, NS, true, true, MINB, QT, SPL, PAGED, MASK>(p, grid, smem, st)
-                : launch_one<D, BN, NS, true, false, MINB, QT, SPL, PAGED, MASK>(p, grid, smem, st);
-  return bf16 ? launch_one<D, BN, NS, false, true, MINB, QT, SPL, PAGED, MASK>(p, grid, smem, st)
-              : launch_one<D, BN, NS, false, false, MINB, QT, SPL, PAGED, MASK>(p, grid, smem, st);
+    return bf16 ? launch_one<D, BN, NS, true, true, MINB, QT, SPL, PAGED, MASK, SK>(p, grid, smem, st)
+                : launch_one<D, BN, NS, true, false, MINB, QT, SPL, PAGED, MASK, SK>(p, grid, smem, st);
+  return bf16 ? launch_one<D, BN, NS, false, true, MINB, QT, SPL, PAGED, MASK, SK>(p, grid, smem, st)
+              : launch_one<D, BN, NS, false, false, MINB, QT, SPL, PAGED, MASK, SK>(p, grid, smem, st);
 }
 
 }  // namespace

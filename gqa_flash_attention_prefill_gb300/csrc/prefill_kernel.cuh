@@ -91,6 +91,15 @@ struct PrefillParams {
   const uint32_t* custom_mask;
   const int32_t* mask_indptr;
   long long total_mask_words;
+  // Balanced split (the SK instantiation): the key tiles of all units, laid
+  // end to end in dealing order, are cut into gridDim.x equal shares, one per
+  // CTA.  A unit cut by share boundaries runs as pieces; each piece writes a
+  // partial to part_o / part_ml slot 2c (CTA c's first piece) or 2c + 1 (its
+  // last) and counts itself, per softmax warp, in sk_count[unit * 4 + warp];
+  // the warp that completes a count merges those rows.  Count words carry
+  // the launch's epoch in their upper 48 bits, so stale words count as zero.
+  unsigned long long* sk_count;
+  unsigned long long epoch;
 };
 
 __host__ __device__ constexpr int pow2_cols(int n) {
@@ -258,6 +267,97 @@ __device__ __forceinline__ void load_kv_tile(const PrefillParams& p, const Unit&
   }
 }
 
+// ---------------------------------------------------------------- balanced split
+// A CTA's share of the key tiles is walked as pieces: the rest of the unit
+// its share starts in (from local tile t0), the whole units after it, and
+// the head of the unit its share ends in.
+struct SkWalk {
+  int u, t0, rem;  // next unit, its first tile, tiles left in the share
+};
+
+// Next piece of the walk: U is its unit with the key range narrowed to the
+// piece's tiles [t0, t1); false when the share is used up.
+__device__ __forceinline__ bool sk_next(const PrefillParams& p, const SeqTab& T, SkWalk& w, int BN,
+                                        int urows, Unit& U) {
+  if (w.rem <= 0) return false;
+  U = decode_unit(p, T, w.u, BN, urows);
+  U.id = w.u;
+  const int t1 = min(U.n_tiles, w.t0 + w.rem);
+  U.kv_lo += w.t0 * BN;
+  U.n_tiles = t1 - w.t0;
+  w.rem -= t1 - w.t0;
+  w.u += 1;
+  w.t0 = 0;
+  return true;
+}
+
+// Share boundaries: CTA c of C takes global tiles [lo(c), lo(c + 1)) with
+// lo(c) = floor(c W / C) = c q + floor(c r / C), q = W / C, r = W % C, in
+// 32-bit arithmetic (c q <= W < 2^31 and c r < C^2 < 2^31 for C < 46341).
+struct SkShares {
+  int C, q, r;
+  __device__ __forceinline__ SkShares(int W, int C_) : C(C_), q(W / C_), r(W - (W / C_) * C_) {}
+  __device__ __forceinline__ int lo(int c) const {
+    return c * q + (int)((unsigned)(c * r) / (unsigned)C);
+  }
+};
+
+// Counts one piece of a unit (for one warp's rows) and returns the count
+// including it.  The word holds epoch << 16 | count; a word tagged with
+// another epoch (a previous launch, or memory never written) counts as zero.
+// Lock-free: a failed compare-and-swap means another piece counted first.
+// After 2^20 failed attempts (not expected: at most a few pieces race) the
+// device status is raised and -1 returned (no merge).
+__device__ __forceinline__ int sk_arrive(unsigned long long* word, unsigned long long epoch,
+                                         unsigned int* status) {
+  unsigned long long old = epoch << 16;
+  for (int n = 0; n < (1 << 20); ++n) {
+    const unsigned long long cnt = (old >> 16) == epoch ? (old & 0xffffull) : 0ull;
+    const unsigned long long got = atomicCAS(word, old, (epoch << 16) | (cnt + 1ull));
+    if (got == old) return (int)(cnt + 1ull);
+    old = got;
+  }
+  atomicOr(status, 1u);  // GQA_DEV_TIMEOUT
+  return -1;
+}
+
+// Exclusive scan of a[0, n) in place by all nthreads threads of the CTA
+// (contiguous segments per thread, warp scans, then the warp totals);
+// a[n] receives the total.  `warp_tot` holds one word per warp.
+__device__ __forceinline__ void cta_exclusive_scan(int32_t* a, int n, int32_t* warp_tot, int tid,
+                                                   int nthreads) {
+  const int per = (n + nthreads - 1) / nthreads;
+  const int i0 = min(tid * per, n), i1 = min(i0 + per, n);
+  int local = 0;
+  for (int i = i0; i < i1; ++i) local += a[i];
+  int incl = local;
+  const int lane = tid & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[tid >> 5] = incl;
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int w = 0; w < nthreads / 32; ++w) {
+      const int v = warp_tot[w];
+      warp_tot[w] = acc;
+      acc += v;
+    }
+    a[n] = acc;
+  }
+  __syncthreads();
+  int acc = warp_tot[tid >> 5] + incl - local;
+  for (int i = i0; i < i1; ++i) {
+    const int v = a[i];
+    a[i] = acc;
+    acc += v;
+  }
+  __syncthreads();
+}
+
 // Custom-mask bits of a 64-key chunk for one query row: bit c is set when key
 // jp0 + c of the extend part (jp0 may be negative: the chunk's first -jp0
 // keys are prefix keys, which the mask does not cover) is kept.  `row` is
@@ -394,14 +494,17 @@ static __device__ __noinline__ void deal_order(const int32_t* keys, int32_t* ord
 }
 
 // SPL: split-KV work items writing partials; PAGED: K/V from a page pool;
-// MASK: the custom mask ANDed into the causal / window mask.  Each is a
-// separate instantiation, so the default kernel carries none of their code.
+// MASK: the custom mask ANDed into the causal / window mask; SK: balanced
+// split (equal shares of all key tiles per CTA, cut units merged in-kernel).
+// Each is a separate instantiation, so the default kernel carries none of
+// their code.
 template <int D, int BN, int NS, bool WIN, bool BF16, int MINB, int QT, bool SPL, bool PAGED,
-          bool MASK = false>
+          bool MASK = false, bool SK = false>
 __global__ void __launch_bounds__(threads_for(QT), MINB)
     prefill_kernel(const __grid_constant__ PrefillParams p) {
   static_assert(D == 64 || D == 128 || D == 256, "head dim");
   static_assert(!MASK || (BN != 96 && !SPL && !PAGED && QT == 1), "custom-mask shapes");
+  static_assert(!SK || (BN != 96 && !SPL && !PAGED && !MASK && QT == 1), "balanced-split shapes");
   static_assert(BN == 64 || BN == 96 || BN == 128, "key tile");
   static_assert(QT == 1 || (QT == 2 && tmem_cols_for(D, BN) <= 256), "query tiles per CTA");
   constexpr int kThr = threads_for(QT);
@@ -559,7 +662,44 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
   // Work items: units, times the split count under split-KV.
   const int n_units = tile_start[nseq] * p.Hkv * (SPL ? p.num_splits : 1);
   if (SPL && blockIdx.x == 0 && tid == 0) p.part_hdr[0] = tile_start[nseq] * p.Hkv;
-  if (blockIdx.x >= n_units) return;  // nothing for this CTA (before any TMEM use)
+  if (!SK && blockIdx.x >= n_units) return;  // nothing for this CTA (before any TMEM use)
+  // Balanced split: the key tiles of every query tile (in dealing order) into
+  // the K/V rings, still unused, their exclusive scan, and this CTA's share:
+  // sk[0] first unit, sk[1] its first tile, sk[2] tiles, sk[3] global index of
+  // the first tile, sk[4] W (the host keeps W below 2^31 and the query tiles
+  // within the rings).
+  int32_t* const sk = scan + 8;
+  if constexpr (SK) {
+    static_assert(kThr / 32 <= 8, "scan words 8..12 hold the share");
+    int32_t* qn = reinterpret_cast<int32_t*>(smem + NQ * QT * kQBytes);
+    const int nq = tile_start[nseq];
+    for (int q = tid; q < nq; q += kThr) qn[q] = decode_unit(p, T, q * p.Hkv, BN, urows).n_tiles;
+    __syncthreads();
+    cta_exclusive_scan(qn, nq, scan, tid, kThr);
+    if (tid == 0) {
+      const int W = p.Hkv * qn[nq], c = blockIdx.x;
+      const SkShares sh(W, (int)gridDim.x);
+      const int lo = sh.lo(c), hi = sh.lo(c + 1);
+      sk[0] = 0;
+      sk[1] = 0;
+      if (hi > lo) {  // query tile holding global tile lo: Hkv qn[a] <= lo < Hkv qn[a + 1]
+        int a = 0, b = nq;
+        while (b - a > 1) {
+          const int mid = (a + b) >> 1;
+          if (p.Hkv * qn[mid] <= lo) a = mid; else b = mid;
+        }
+        const int off = lo - p.Hkv * qn[a], n = qn[a + 1] - qn[a];  // n >= 1
+        sk[0] = a * p.Hkv + off / n;
+        sk[1] = off % n;
+      }
+      sk[2] = hi - lo;
+      sk[3] = lo;
+      sk[4] = W;
+    }
+    fence_proxy_async_smem();  // the rings were written here; TMA writes them next
+    __syncthreads();
+    if (sk[2] <= 0) return;  // an empty share (fewer tiles than CTAs)
+  }
 
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(misc), kTmemCols);
@@ -581,10 +721,17 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
       uint32_t nq = 0, nk[NS];
       for (int s = 0; s < NS; ++s) nk[s] = 0u;
       uint32_t itk = 0;
+      SkWalk wk{};
+      if constexpr (SK) wk = SkWalk{sk[0], sk[1], sk[2]};
       for (int kk = 0;; ++kk) {
-        const int uk = unit_of(kk);
-        if (uk >= n_units) break;
-        const Unit U = decode_item<SPL>(p, T, uk, BN, urows);
+        Unit U;
+        if constexpr (SK) {
+          if (!sk_next(p, T, wk, BN, urows, U)) break;
+        } else {
+          const int uk = unit_of(kk);
+          if (uk >= n_units) break;
+          U = decode_item<SPL>(p, T, uk, BN, urows);
+        }
         if (SPL && U.n_tiles == 0) continue;  // empty split: no loads, no Q buffer
         const uint32_t qb = nq % NQ;
         if (!wait_bounded(sBar + 8u * (B::kQEmpty + qb), ((nq / NQ) & 1u) ^ 1u, abort_flag,
@@ -626,10 +773,17 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
       for (int s = 0; s < NS; ++s) nv[s] = 0u;
       uint32_t itv = 0;
       bool ok = true;
+      SkWalk wk{};
+      if constexpr (SK) wk = SkWalk{sk[0], sk[1], sk[2]};
       for (int kv = 0; ok; ++kv) {
-        const int uv = unit_of(kv);
-        if (uv >= n_units) break;
-        const Unit U = decode_item<SPL>(p, T, uv, BN, urows);
+        Unit U;
+        if constexpr (SK) {
+          if (!sk_next(p, T, wk, BN, urows, U)) break;
+        } else {
+          const int uv = unit_of(kv);
+          if (uv >= n_units) break;
+          U = decode_item<SPL>(p, T, uv, BN, urows);
+        }
         for (int j = 0; j < U.n_tiles; ++j, ++itv) {
           const uint32_t s = itv % NS, ph = (itv / NS) & 1u;
           if (!(ok = wait_bounded(sBar + 8u * (B::kVEmpty + s), ph ^ 1u, abort_flag, p.status, tmo)))
@@ -690,14 +844,25 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
     };
     uint32_t it = 0, uc = 0;
     bool ok = true;
-    int u = unit_of(0);
+    int u;
     Unit Un;
-    if (u < n_units) Un = decode_item<SPL>(p, T, u, BN, urows);
+    SkWalk wk{};
+    if constexpr (SK) {  // u: 0 while a piece is decoded ahead, n_units after the last
+      wk = SkWalk{sk[0], sk[1], sk[2]};
+      u = sk_next(p, T, wk, BN, urows, Un) ? 0 : n_units;
+    } else {
+      u = unit_of(0);
+      if (u < n_units) Un = decode_item<SPL>(p, T, u, BN, urows);
+    }
     for (int k = 0; ok && u < n_units; ++k) {
       const Unit U = Un;  // decoded one unit ahead: its loads overlap this unit
-      const int u_next = unit_of(k + 1);
-      if (u_next < n_units) Un = decode_item<SPL>(p, T, u_next, BN, urows);
-      u = u_next;
+      if constexpr (SK) {
+        u = sk_next(p, T, wk, BN, urows, Un) ? 0 : n_units;
+      } else {
+        const int u_next = unit_of(k + 1);
+        if (u_next < n_units) Un = decode_item<SPL>(p, T, u_next, BN, urows);
+        u = u_next;
+      }
       if (SPL && U.n_tiles == 0) continue;  // empty split: nothing to issue
       const uint32_t qb = uc % NQ;
       if (!(ok = wait_all(sBar + 8u * (B::kQFull + qb), (uc / NQ) & 1u))) break;
@@ -749,11 +914,18 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
     constexpr bool split = SPL;
     const int part_rows = QT * 128;  // partial rows per work item
     const int rr = sub * 128 + r;     // this thread's partial row
-    int u = unit_of(0);
+    int u;
     Unit Un;
     float sink_next = 0.f;
+    SkWalk wk{};
+    if constexpr (SK) {  // u: 0 while a piece is decoded ahead, n_units after the last
+      wk = SkWalk{sk[0], sk[1], sk[2]};
+      u = sk_next(p, T, wk, BN, urows, Un) ? 0 : n_units;
+    } else {
+      u = unit_of(0);
+    }
     if (u < n_units) {
-      Un = decode_item<SPL>(p, T, u, BN, urows);
+      if constexpr (!SK) Un = decode_item<SPL>(p, T, u, BN, urows);
       if (p.sinks != nullptr) sink_next = __ldg(p.sinks + Un.g * p.G + r % p.G);
     }
     for (int k = 0; ok && u < n_units; ++k) {
@@ -762,9 +934,13 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
       const Unit U = Un;
       const int cur_u = u;
       const float sink = sink_next;
-      u = unit_of(k + 1);
+      if constexpr (SK) {
+        u = sk_next(p, T, wk, BN, urows, Un) ? 0 : n_units;
+      } else {
+        u = unit_of(k + 1);
+      }
       if (u < n_units) {
-        Un = decode_item<SPL>(p, T, u, BN, urows);
+        if constexpr (!SK) Un = decode_item<SPL>(p, T, u, BN, urows);
         if (p.sinks != nullptr) sink_next = __ldg(p.sinks + Un.g * p.G + r % p.G);
       }
       if (split && leader && sub == 0) {  // where the merge writes this unit's rows
@@ -975,6 +1151,138 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
                                                  ((it - 1u) / NP) & 1u, abort_flag, p.status, tmo));
       if (!ok) break;
       tc_fence_after();
+      if constexpr (SK) {
+        // A cut unit runs as pieces: the one holding the unit's first tiles
+        // (the last piece of its share) owns the unit, the later ones (each
+        // the first piece of a later share) contribute.
+        const int t0 = k == 0 ? sk[1] : 0;
+        const int n_all = kv_range(U.P, U.q0, U.q_last, win, BN).n_tiles;
+        if (t0 != 0 || U.n_tiles != n_all) {
+          // A piece of a cut unit.  Its partial (O relative to m, unnormalised,
+          // and (m, l)) goes to slot 2c (this CTA's first piece) or 2c + 1 (its
+          // last); then each warp counts the piece for its 32 rows, and the
+          // warp whose count completes the unit's pieces merges those rows
+          // with the log-sum-exp combine and writes them.  No CTA waits on
+          // another: every partial is visible before the count that includes it.
+          const int slot = 2 * (int)blockIdx.x + (k == 0 ? 0 : 1);
+          float4* po = reinterpret_cast<float4*>(p.part_o) + (size_t)slot * (D / 4) * 128;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(t_lane + kColO + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              po[(size_t)(c * 8 + i) * 128 + r] =
+                  make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                              __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+          }
+          reinterpret_cast<float2*>(p.part_ml)[(size_t)slot * 128 + r] = make_float2(m, l);
+          fence_acq_rel_gpu();  // release: the partial before the count that publishes it
+          tc_fence_before();
+          __syncwarp();
+          if (leader) mbar_arrive(sBar + 8u * (B::kQEmpty + qb));  // nothing staged in Q
+          unsigned long long* word = p.sk_count + (size_t)U.id * 4 + (warp & 3);
+          int cnt = 0;
+          if (lane == 0) {
+            cnt = sk_arrive(word, p.epoch, p.status);
+            fence_acq_rel_gpu();  // acquire: the other pieces' partials after their counts
+          }
+          cnt = __shfl_sync(0xffffffffu, cnt, 0);
+          // The shares c0..c1 that hold the unit's tiles [gu, gu + n_all): walk
+          // from this CTA's share to the ones holding the unit's first and last.
+          const SkShares sh(sk[4], (int)gridDim.x);
+          const int gu = sk[3] + (int)(it - (uint32_t)U.n_tiles) - t0;  // the unit's first tile
+          int c0 = (int)blockIdx.x, c1 = (int)blockIdx.x;
+          while (sh.lo(c0) > gu) --c0;
+          while (sh.lo(c1 + 1) <= gu + n_all - 1) ++c1;
+          auto nonempty = [&](int c) { return sh.lo(c + 1) > sh.lo(c); };
+          int npieces = 0;
+          for (int c = c0; c <= c1; ++c) npieces += nonempty(c) ? 1 : 0;
+          if (cnt != npieces) continue;  // another piece merges these rows
+          // Merge in share order c0..c1 whichever piece merges (this piece's
+          // values equal its partial's), so the result is the same run to run:
+          // per 32 output columns, each piece's (m, l) and O loaded together
+          // (one round trip to L2 per piece) and combined online against a
+          // running maximum.
+          auto slot_of = [&](int c) { return 2 * c + (sh.lo(c) >= gu ? 0 : 1); };
+          const bool has_x = (p.sinks != nullptr) || (p.smooth != 0);
+          const float ms = sink * kLog2e;  // 0 in smooth mode
+          const float2* pml = reinterpret_cast<const float2*>(p.part_ml);
+          const bool valid = pl <= qls;
+          const size_t orow = (size_t)(U.q_row0 + sub * p.rows + r / p.G) * p.Hq + h;
+          uint16_t* op = reinterpret_cast<uint16_t*>(p.out) + orow * D;
+          float lse2 = -INFINITY;
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            float acc[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+            float M = -INFINITY, dsum = 0.f;
+            // Uniform over the warp (tcgen05.ld is warp-wide); a piece that saw
+            // no key of a row has m = -inf there and adds nothing.
+            for (int c = c0; c <= c1; ++c) {
+              if (!nonempty(c)) continue;
+              float2 v;
+              uint32_t x[32];
+              if (c == (int)blockIdx.x) {
+                v = make_float2(m, l);
+                tmem_ld32(t_lane + kColO + cc * 32, x);
+                tmem_wait_ld();
+              } else {
+                const size_t sc = (size_t)slot_of(c);
+                const float4* src = reinterpret_cast<const float4*>(p.part_o) + sc * (D / 4) * 128;
+                v = __ldcg(pml + sc * 128 + r);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float4 f = __ldcg(src + (size_t)(cc * 8 + i) * 128 + r);
+                  x[4 * i] = __float_as_uint(f.x);
+                  x[4 * i + 1] = __float_as_uint(f.y);
+                  x[4 * i + 2] = __float_as_uint(f.z);
+                  x[4 * i + 3] = __float_as_uint(f.w);
+                }
+              }
+              float a_run = 1.f, a_new = 0.f;
+              if (v.x != -INFINITY) {
+                if (v.x > M) {
+                  a_run = (M == -INFINITY) ? 0.f : ex2(M - v.x);
+                  a_new = 1.f;
+                  M = v.x;
+                } else {
+                  a_new = ex2(v.x - M);
+                }
+              }
+              dsum = dsum * a_run + v.y * a_new;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) acc[i] = acc[i] * a_run + __uint_as_float(x[i]) * a_new;
+            }
+            // Fold the sink in once: den against mf = max(M, sink log2 e).
+            float scl = 0.f;
+            if (M != -INFINITY) {
+              const float mf = has_x ? fmaxf(M, ms) : M;
+              const float a = ex2(M - mf);
+              float den = dsum * a + (has_x ? ex2(ms - mf) : 0.f);
+              den = fmaxf(den, 1e-30f);
+              scl = a / den;
+              lse2 = mf + log2f(den);
+            }
+            if (valid) {
+              uint4* dst = reinterpret_cast<uint4*>(op + cc * 32);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(pack2<BF16>(acc[8 * i] * scl, acc[8 * i + 1] * scl),
+                                    pack2<BF16>(acc[8 * i + 2] * scl, acc[8 * i + 3] * scl),
+                                    pack2<BF16>(acc[8 * i + 4] * scl, acc[8 * i + 5] * scl),
+                                    pack2<BF16>(acc[8 * i + 6] * scl, acc[8 * i + 7] * scl));
+            }
+          }
+          if (valid && p.lse != nullptr) p.lse[orow] = lse2 * kLn2;
+          // Every piece has counted: zero the count, so that a replay of this
+          // very launch (same epoch, e.g. from a CUDA graph) starts from zero.
+          if (lane == 0) *word = p.epoch << 16;
+          continue;
+        }
+      }
       if constexpr (split) {
         // Partial of one key range: O relative to m, unnormalised, with (m, l);
         // float4 (c4, row) order so that a warp's stores are contiguous.

@@ -51,6 +51,11 @@ __device__ __forceinline__ void grid_dep_wait() {
 __device__ __forceinline__ void grid_dep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// Acquire-release fence at GPU scope: with a relaxed atomic after it (before
+// it) it forms a release (acquire) pattern.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));

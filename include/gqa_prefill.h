@@ -198,6 +198,9 @@ GQA_API int gqa_flash_prefill_paged(const void* q, const void* k_pages,
                                     const float* sinks, int smooth_softmax,
                                     void* out, float* lse, void* stream);
 
+/* num_splits value selecting the balanced split (see below). */
+#define GQA_SPLITS_BALANCED (-1)
+
 /*
  * gqa_flash_prefill_splitkv -- the same operation as gqa_flash_prefill, with
  * each work unit's key tiles divided into num_splits contiguous ranges
@@ -209,19 +212,35 @@ GQA_API int gqa_flash_prefill_paged(const void* q, const void* k_pages,
  * that SGLang PR #34468 ("gfx950 SWA prefix trim") uses for its
  * context-parallel path.  The result equals the unsplit call up to rounding.
  *
+ * With num_splits = GQA_SPLITS_BALANCED the call is one kernel whose
+ * resident CTAs take equal shares of all the call's key tiles (the units
+ * laid end to end in the order they are dealt), so that no CTA idles while
+ * others finish a last wave: for calls whose units do not divide evenly over
+ * the CTAs (a 512-token chunk's 256 units on 304 resident CTAs).  A unit that
+ * share boundaries cut runs as pieces on consecutive CTAs; each piece writes
+ * an fp32 partial and counts itself with an atomic, and the piece that
+ * completes the count merges the unit's partials (the same log-sum-exp merge,
+ * in a fixed order, so the result is the same run to run) and writes the
+ * rows.  No CTA waits on another.  Declined (GQA_ERR_UNSUPPORTED) when one
+ * launch has more query tiles than the kernel's shared-memory scratch holds
+ * (about 16,000 at d = 64) or more than 2^31 key tiles in all.
+ *
  *   num_splits       0: the library's choice (splits only when the units fill
  *                    less than half the resident CTAs), else 1..16; 1 is the
- *                    unsplit kernel and needs no workspace.
+ *                    unsplit kernel and needs no workspace;
+ *                    GQA_SPLITS_BALANCED: the balanced split.
  *   workspace        device memory owned by the caller, 256-byte aligned, at
  *                    least the size gqa_prefill_splitkv_workspace() reports
  *                    for the same shapes and num_splits; only scratch (its
- *                    contents before and after the call are meaningless), and
- *                    must not be shared by calls that may run concurrently.
+ *                    contents before and after the call are meaningless: the
+ *                    balanced split's count words carry a per-launch tag, and
+ *                    words with another tag count as zero), and must not be
+ *                    shared by calls that may run concurrently.
  *   workspace_bytes  its size.
  *
  * Other arguments, layouts and return codes as gqa_flash_prefill; a missing
  * or too small workspace returns GQA_ERR_INVALID before any launch.  Two
- * kernels are enqueued on `stream`.
+ * kernels are enqueued on `stream` (one for the balanced split).
  */
 GQA_API int gqa_flash_prefill_splitkv(const void* q, const void* k, const void* v,
                               const int32_t* cu_seqlens_q,
@@ -268,7 +287,9 @@ GQA_API int gqa_flash_prefill_splitkv_noalloc(const void* q, const void* k, cons
 /*
  * Host only: the split count gqa_flash_prefill_splitkv will use for these
  * shapes and num_splits (0 = the library's choice) in *splits_used, and the
- * workspace it needs in *bytes (0 when the call does not split).  Returns
+ * workspace it needs in *bytes (0 when the call does not split).  For
+ * GQA_SPLITS_BALANCED, *splits_used is GQA_SPLITS_BALANCED and *bytes covers
+ * two partial tiles per resident CTA plus 32 bytes per work unit.  Returns
  * GQA_OK, GQA_ERR_INVALID or GQA_ERR_UNSUPPORTED as gqa_prefill_plan.
  */
 GQA_API int gqa_prefill_splitkv_workspace(int num_seqs, int total_q, int max_seqlen_q,

@@ -106,7 +106,7 @@ def _call_noalloc(lib, **over):
     (dict(scale=0.0), -1),
     (dict(sinks=FAKE, smooth=1), -1),
     (dict(splits=17), -1),
-    (dict(splits=-1), -1),
+    (dict(splits=-2), -1),
     (dict(q=None), -1),
     (dict(d=96), -2),
     # arguments are checked before the empty-work early return
@@ -184,6 +184,27 @@ def test_split_count_choice_is_host_only(lib):
     assert used > 1 and nbytes > 0
     used, nbytes = pkg.splitkv_workspace(1, 64, 64, 64, 8, 64, "bf16", 0, 16)
     assert used == 16 and nbytes > 0
+
+
+def test_balanced_split_workspace_is_host_only(lib):
+    """The balanced split's workspace from shapes alone: two partial tiles
+    per resident CTA plus four count words per unit; a launch with more query
+    tiles than the kernel's shared-memory scratch holds is declined; split
+    counts below GQA_SPLITS_BALANCED are invalid."""
+    import gqa_flash_attention_prefill_gb300 as pkg
+    used, nbytes = pkg.splitkv_workspace(1, 512, 512, 64, 8, 64, "bf16", 0, pkg.SPLITS_BALANCED)
+    p = pkg.plan(1, 512, 512, 64, 8, 64, "bf16", 0)
+    slots = p["grid"] if p["grid"] < p["max_units"] else None
+    assert used == pkg.SPLITS_BALANCED and nbytes >= 2 * 128 * 64 * 4 * 2
+    if slots is not None:
+        assert nbytes >= 2 * slots * 128 * 64 * 4
+    used2, nbytes2 = pkg.splitkv_workspace(2, 4096, 2048, 64, 8, 64, "bf16", 0,
+                                           pkg.SPLITS_BALANCED)
+    assert used2 == pkg.SPLITS_BALANCED and nbytes2 > nbytes  # more units, more count words
+    with pytest.raises(pkg.GQAError):  # 2^20 queries: 65,536 query tiles per launch
+        pkg.splitkv_workspace(1, 1 << 20, 1 << 20, 64, 8, 64, "bf16", 0, pkg.SPLITS_BALANCED)
+    with pytest.raises(pkg.GQAError):
+        pkg.splitkv_workspace(1, 512, 512, 64, 8, 64, "bf16", 0, -2)
 
 
 def _call_masked(lib, **over):
