@@ -436,11 +436,18 @@ def step_workspace(pkg, mode):
     return torch.empty(nbytes, dtype=torch.uint8, device="cuda")
 
 
-def step_prepare(pkg, batch, kind, mode, ws, out, lse, stream):
+# --balanced long: the prefix from which a full-causal chunk call takes the
+# balanced split (measured crossover on GB300: about chunk 20 of 32).
+LONG_PREFIX = 10240
+
+
+def step_prepare(pkg, batch, kind, mode, ws, out, lse, stream, prefix=0):
     """A prepared call of the 16k step: the plain entry point, or the
-    balanced split for the full-causal calls (`mode` "full") or all calls
-    ("all")."""
-    bal = mode == "all" or (mode == "full" and kind == "full_causal")
+    balanced split for the full-causal calls (`mode` "full"), for the
+    full-causal calls over at least LONG_PREFIX cached tokens ("long"), or
+    for all calls ("all")."""
+    bal = (mode == "all" or (mode == "full" and kind == "full_causal")
+           or (mode == "long" and kind == "full_causal" and prefix >= LONG_PREFIX))
     return pkg.prepare(batch, out=out, lse=lse, stream=stream,
                        num_splits=pkg.SPLITS_BALANCED if bal else None,
                        workspace=ws if bal else None)
@@ -464,7 +471,7 @@ def run_oss20b(args, rank, world):
         c, layer = cl["chunk"], cl["layer"]
         cl["run"] = step_prepare(pkg, cl["batch"], cl["kind"], args.balanced, ws,
                                  out[layer, c * L:(c + 1) * L], lse[layer, c * L:(c + 1) * L],
-                                 stream)
+                                 stream, prefix=c * L)
     flops = sum(cl["flops"] for cl in calls)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
 
@@ -606,7 +613,8 @@ def run_profile(args):
             b = st.call(SEQ // CHUNK - 1, layer)
             kind = "window_128" if b.window > 0 else "full_causal"
             step_prepare(pkg, b, kind, args.balanced, ws, torch.empty_like(b.q),
-                         torch.empty(b.q.shape[:2], dtype=torch.float32, device="cuda"), stream)()
+                         torch.empty(b.q.shape[:2], dtype=torch.float32, device="cuda"), stream,
+                         prefix=SEQ - CHUNK)()
         n = 2
     else:
         st, metas, calls = oss20b_setup()
@@ -616,7 +624,8 @@ def run_profile(args):
         ws = step_workspace(pkg, args.balanced)
         runs = [step_prepare(pkg, cl["batch"], cl["kind"], args.balanced, ws,
                              out[cl["layer"], cl["chunk"] * L:(cl["chunk"] + 1) * L],
-                             lse[cl["layer"], cl["chunk"] * L:(cl["chunk"] + 1) * L], stream)
+                             lse[cl["layer"], cl["chunk"] * L:(cl["chunk"] + 1) * L], stream,
+                             prefix=cl["chunk"] * L)
                 for cl in calls]
         for _ in range(args.warmup + 1):
             for r in runs:
@@ -628,10 +637,12 @@ def run_profile(args):
     print(f"profile run done: {n} prefill launches", flush=True)
 
 
-def bench_config(world, balanced="none"):
+def bench_config(world, balanced="long"):
     entry = {"none": "gqa_flash_prefill",
              "full": "gqa_flash_prefill_splitkv (balanced split) for the full-causal calls, "
                      "gqa_flash_prefill for the window-128 calls",
+             "long": f"gqa_flash_prefill_splitkv (balanced split) for the full-causal calls "
+                     f"over >= {LONG_PREFIX} cached tokens, gqa_flash_prefill for the others",
              "all": "gqa_flash_prefill_splitkv (balanced split)"}[balanced]
     return {"workload": WORKLOAD, "global_batch": world, "seq_len": SEQ, "chunk_len": CHUNK,
             "layers": LAYERS, "calls_per_step": LAYERS * (SEQ // CHUNK),
@@ -677,7 +688,7 @@ def oss20b_e2e(args, st, metas, calls, out, lse, stream, world, flops, ws=None):
         runs = [[step_prepare(pkg, s_.call(c, layer, m_[c]),
                               "window_128" if s_.windows[layer] > 0 else "full_causal",
                               args.balanced, ws, o_[layer, c * L:(c + 1) * L],
-                              l_[layer, c * L:(c + 1) * L], stream)
+                              l_[layer, c * L:(c + 1) * L], stream, prefix=c * L)
                  for layer in range(n_l)] for c in range(n_c)]
         sets.append({"st": s_, "metas": m_, "out": o_, "lse": l_, "runs": runs,
                      "in_ready": [torch.cuda.Event() for _ in range(n_c)],
@@ -1190,9 +1201,10 @@ def main():
     ap.add_argument("--splits", type=int, default=-1,
                     help="supplementary workloads: -1 the plain entry point; 0 split-KV with "
                          "the library's split count; k >= 1 split-KV with k splits")
-    ap.add_argument("--balanced", choices=["none", "full", "all"], default="none",
+    ap.add_argument("--balanced", choices=["none", "long", "full", "all"], default="long",
                     help="16k prefill: the balanced split (gqa_flash_prefill_splitkv with "
-                         "GQA_SPLITS_BALANCED) for no call, the full-causal calls, or all calls")
+                         "GQA_SPLITS_BALANCED) for no call, the full-causal calls over long "
+                         "prefixes, all full-causal calls, or all calls")
     ap.add_argument("--profile", choices=["step", "chunk31", "pair"], default=None,
                     help="untimed run for an ncu capture: the warm-up steps plus one step of "
                          "the 16k prefill, chunk 31's two calls, or the layer pair's two "

@@ -304,13 +304,15 @@ struct SkShares {
 
 // Counts one piece of a unit (for one warp's rows) and returns the count
 // including it.  The word holds epoch << 16 | count; a word tagged with
-// another epoch (a previous launch, or memory never written) counts as zero.
+// another epoch (memory never written, or a launch that did not finish)
+// counts as zero, and so does 0, the value a completed count is reset to.
+// `guess` is the word's expected value (0: this piece is expected first).
 // Lock-free: a failed compare-and-swap means another piece counted first.
 // After 2^20 failed attempts (not expected: at most a few pieces race) the
 // device status is raised and -1 returned (no merge).
 __device__ __forceinline__ int sk_arrive(unsigned long long* word, unsigned long long epoch,
-                                         unsigned int* status) {
-  unsigned long long old = epoch << 16;
+                                         unsigned long long guess, unsigned int* status) {
+  unsigned long long old = guess;
   for (int n = 0; n < (1 << 20); ++n) {
     const unsigned long long cnt = (old >> 16) == epoch ? (old & 0xffffull) : 0ull;
     const unsigned long long got = atomicCAS(word, old, (epoch << 16) | (cnt + 1ull));
@@ -445,10 +447,13 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity,
 // sort is a bitonic sort, descending, of the composites key * 512 +
 // (511 - index) (keys clamped to 2^22 - 1; the padding up to a power of two
 // holds -1 and sorts last).  Called by every thread of the CTA; `scratch`
-// is two shared words.  Kept out of line, so that the kernel body, and with
-// it the placement of its hot loops, does not depend on it.
-static __device__ __noinline__ void deal_order(const int32_t* keys, int32_t* order, int32_t* scratch,
-                                        int nseq, int tid, int nthreads) {
+// is two shared words.  deal_order keeps it out of line, so that the kernel
+// body, and with it the placement of its hot loops, does not depend on it;
+// the paged instantiation inlines it (a call there measured 10% slower on
+// 16-token pages, where the page lookups run on the producer warp).
+__device__ __forceinline__ void deal_order_body(const int32_t* keys, int32_t* order,
+                                                int32_t* scratch, int nseq, int tid,
+                                                int nthreads) {
   if (tid == 0) {
     scratch[0] = 0x7fffffff;
     scratch[1] = -1;
@@ -491,6 +496,10 @@ static __device__ __noinline__ void deal_order(const int32_t* keys, int32_t* ord
   __syncthreads();
   for (int r = tid; r < nseq; r += nthreads) order[r] = kMaxSeqs - 1 - (order[r] & (kMaxSeqs - 1));
   __syncthreads();
+}
+static __device__ __noinline__ void deal_order(const int32_t* keys, int32_t* order, int32_t* scratch,
+                                               int nseq, int tid, int nthreads) {
+  deal_order_body(keys, order, scratch, nseq, tid, nthreads);
 }
 
 // SPL: split-KV work items writing partials; PAGED: K/V from a page pool;
@@ -616,7 +625,12 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
   __syncthreads();
   // Costliest sequences first (deal_order); one call whatever the batch, so
   // the kernel body stays the same size.
-  if (nseq > 1) deal_order(tile_start, seq_order, scan + 14, nseq, tid, kThr);
+  if (nseq > 1) {
+    if constexpr (PAGED)
+      deal_order_body(tile_start, seq_order, scan + 14, nseq, tid, kThr);
+    else
+      deal_order(tile_start, seq_order, scan + 14, nseq, tid, kThr);
+  }
   // Units per sequence in dealing order, then their exclusive scan: warp
   // scans, then warp totals.  tile_start[r] is the first unit (of one KV
   // head) of the r-th sequence dealt.
@@ -1158,39 +1172,15 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
         const int t0 = k == 0 ? sk[1] : 0;
         const int n_all = kv_range(U.P, U.q0, U.q_last, win, BN).n_tiles;
         if (t0 != 0 || U.n_tiles != n_all) {
-          // A piece of a cut unit.  Its partial (O relative to m, unnormalised,
-          // and (m, l)) goes to slot 2c (this CTA's first piece) or 2c + 1 (its
-          // last); then each warp counts the piece for its 32 rows, and the
-          // warp whose count completes the unit's pieces merges those rows
-          // with the log-sum-exp combine and writes them.  No CTA waits on
-          // another: every partial is visible before the count that includes it.
-          const int slot = 2 * (int)blockIdx.x + (k == 0 ? 0 : 1);
-          float4* po = reinterpret_cast<float4*>(p.part_o) + (size_t)slot * (D / 4) * 128;
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(t_lane + kColO + c * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              po[(size_t)(c * 8 + i) * 128 + r] =
-                  make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
-                              __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
-          }
-          reinterpret_cast<float2*>(p.part_ml)[(size_t)slot * 128 + r] = make_float2(m, l);
-          fence_acq_rel_gpu();  // release: the partial before the count that publishes it
-          tc_fence_before();
-          __syncwarp();
-          if (leader) mbar_arrive(sBar + 8u * (B::kQEmpty + qb));  // nothing staged in Q
-          unsigned long long* word = p.sk_count + (size_t)U.id * 4 + (warp & 3);
-          int cnt = 0;
-          if (lane == 0) {
-            cnt = sk_arrive(word, p.epoch, p.status);
-            fence_acq_rel_gpu();  // acquire: the other pieces' partials after their counts
-          }
-          cnt = __shfl_sync(0xffffffffu, cnt, 0);
-          // The shares c0..c1 that hold the unit's tiles [gu, gu + n_all): walk
-          // from this CTA's share to the ones holding the unit's first and last.
+          // A piece of a cut unit.  Each warp counts the piece for its 32 rows
+          // in the unit's count word, after publishing its partial (O relative
+          // to m, unnormalised, and (m, l)) to slot 2c (this CTA's first piece)
+          // or 2c + 1 (its last); the warp whose count completes the unit's
+          // pieces merges those rows with the log-sum-exp combine and writes
+          // them.  No CTA waits on another.  The piece holding the unit's first
+          // tiles (the last piece of its CTA, normally the last to finish) first
+          // tries to complete the count without publishing: if every other
+          // piece has counted, it merges at once.
           const SkShares sh(sk[4], (int)gridDim.x);
           const int gu = sk[3] + (int)(it - (uint32_t)U.n_tiles) - t0;  // the unit's first tile
           int c0 = (int)blockIdx.x, c1 = (int)blockIdx.x;
@@ -1199,7 +1189,42 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
           auto nonempty = [&](int c) { return sh.lo(c + 1) > sh.lo(c); };
           int npieces = 0;
           for (int c = c0; c <= c1; ++c) npieces += nonempty(c) ? 1 : 0;
-          if (cnt != npieces) continue;  // another piece merges these rows
+          unsigned long long* word = p.sk_count + (size_t)U.id * 4 + (warp & 3);
+          unsigned long long seen = 0ull;  // lane 0: the count word as last read
+          int last = 0;
+          if (t0 == 0 && lane == 0) {
+            const unsigned long long want = (p.epoch << 16) | (unsigned long long)(npieces - 1);
+            seen = atomicCAS(word, want, want + 1ull);
+            last = seen == want;
+          }
+          last = __shfl_sync(0xffffffffu, last, 0);
+          if (!last) {
+            const int slot = 2 * (int)blockIdx.x + (k == 0 ? 0 : 1);
+            float4* po = reinterpret_cast<float4*>(p.part_o) + (size_t)slot * (D / 4) * 128;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(t_lane + kColO + c * 32, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                po[(size_t)(c * 8 + i) * 128 + r] =
+                    make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+            }
+            reinterpret_cast<float2*>(p.part_ml)[(size_t)slot * 128 + r] = make_float2(m, l);
+            fence_acq_rel_gpu();  // release: the partial before the count that publishes it
+            __syncwarp();
+            int cnt = 0;
+            if (lane == 0) cnt = sk_arrive(word, p.epoch, seen, p.status);
+            last = __shfl_sync(0xffffffffu, cnt == npieces ? 1 : 0, 0);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (leader) mbar_arrive(sBar + 8u * (B::kQEmpty + qb));  // nothing staged in Q
+          if (!last) continue;  // another piece merges these rows
+          if (lane == 0) fence_acq_rel_gpu();  // acquire: the other pieces' partials
+          __syncwarp();
           // Merge in share order c0..c1 whichever piece merges (this piece's
           // values equal its partial's), so the result is the same run to run:
           // per 32 output columns, each piece's (m, l) and O loaded together
@@ -1277,9 +1302,10 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
             }
           }
           if (valid && p.lse != nullptr) p.lse[orow] = lse2 * kLn2;
-          // Every piece has counted: zero the count, so that a replay of this
-          // very launch (same epoch, e.g. from a CUDA graph) starts from zero.
-          if (lane == 0) *word = p.epoch << 16;
+          // Every piece has counted: zero the word (count 0 under any epoch),
+          // so that the next launch, or a replay of this one (same epoch, e.g.
+          // from a CUDA graph), starts from zero.
+          if (lane == 0) *word = 0ull;
           continue;
         }
       }
