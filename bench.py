@@ -425,6 +425,19 @@ def oss20b_setup(device="cuda", num_layers=LAYERS, seq=SEQ, chunk=CHUNK):
     return st, metas, calls
 
 
+def split_request(pkg, splits):
+    """num_splits for --splits: None (the plain entry point), an int >= 0, or
+    SPLITS_BALANCED."""
+    if splits in (None, "none"):
+        return None
+    if splits == "balanced":
+        return pkg.SPLITS_BALANCED
+    k = int(splits)
+    if k < 0:
+        raise ValueError("--splits takes none, balanced or an integer >= 0")
+    return k
+
+
 def step_workspace(pkg, mode):
     """The one workspace the 16k step's balanced-split calls share (they run
     in stream order), or None when `mode` is "none"."""
@@ -976,13 +989,15 @@ def run_workload(args, rank, world):
     lses = [torch.empty(b.q.shape[:2], dtype=torch.float32, device=dev) for b in calls]
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    # --splits >= 0: the split-KV entry point (0 = the library's choice), with a
-    # workspace per call allocated here, outside the timed region.
+    # --splits k (k >= 0) or balanced: the split-KV entry point (0 = the
+    # library's choice; balanced = GQA_SPLITS_BALANCED), with a workspace per
+    # call allocated here, outside the timed region.
+    split_req = split_request(pkg, args.splits)
     splits_used, workspaces = [], []
-    if args.splits >= 0:
+    if split_req is not None:
         for b in calls:
             used, nbytes = pkg.splitkv_workspace(b.num_seqs, b.total_q, b.max_seqlen_q, b.hq,
-                                                 b.hkv, b.d, b.dtype_name, b.window, args.splits)
+                                                 b.hkv, b.d, b.dtype_name, b.window, split_req)
             splits_used.append(used)
             workspaces.append(torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev))
 
@@ -996,8 +1011,8 @@ def run_workload(args, rank, world):
                 pkg.prefill_masked(b, masks[i][0], masks[i][1], out=o, lse=l, stream=stream)
             elif args.paged > 0:
                 pkg.prefill_paged(paged_calls[i], out=o, lse=l, stream=stream)
-            elif args.splits >= 0:
-                pkg.prefill_splitkv(b, num_splits=args.splits, workspace=workspaces[i], out=o,
+            elif split_req is not None:
+                pkg.prefill_splitkv(b, num_splits=split_req, workspace=workspaces[i], out=o,
                                     lse=l, stream=stream)
             else:
                 pkg.prefill(b, out=o, lse=l, stream=stream)
@@ -1042,7 +1057,7 @@ def run_workload(args, rank, world):
                        "entry": (f"gqa_flash_prefill_paged, page_size {args.paged}"
                                  if args.paged > 0 else
                                  ("gqa_flash_prefill_splitkv, splits " + str(splits_used))
-                                 if args.splits >= 0 else "gqa_flash_prefill")},
+                                 if split_req is not None else "gqa_flash_prefill")},
             "tokens_per_s": round(world * tokens / (ms_step * 1e-3), 1),
             "pct_of_bf16_peak": round(100.0 * value / (world * peaks["bf16_tflops"]), 2),
             "gpu_launches": len(calls) * steps + sum(1 for s_ in splits_used if s_ > 1) * steps,
@@ -1198,9 +1213,10 @@ def main():
                          "(0: contiguous)")
     ap.add_argument("--grid-steps", type=int, default=10,
                     help="ragged_grid: timed calls per cell (capped by --steps)")
-    ap.add_argument("--splits", type=int, default=-1,
-                    help="supplementary workloads: -1 the plain entry point; 0 split-KV with "
-                         "the library's split count; k >= 1 split-KV with k splits")
+    ap.add_argument("--splits", default="none",
+                    help="supplementary workloads: none, the plain entry point; 0, split-KV "
+                         "with the library's split count; k >= 1, split-KV with k splits; "
+                         "balanced, the balanced split")
     ap.add_argument("--balanced", choices=["none", "long", "full", "all"], default="long",
                     help="16k prefill: the balanced split (gqa_flash_prefill_splitkv with "
                          "GQA_SPLITS_BALANCED) for no call, the full-causal calls over long "

@@ -730,12 +730,16 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
   // tiles, lane 1 walks the same tiles loading V.  K therefore runs as far
   // ahead as its ring allows (a K slot frees when its QK^T is done), however
   // late a V slot frees (when its PV is done).
-  if (warp == kProdWarp && PAGED) {
-    // Paged KV: one lane issues Q, K and V in the order the MMA warp consumes
-    // them (a unit's Q, K0, K1, V0, K2, V1, ..., its last V, then the next
-    // unit's Q), so every wait is for a slot freed by an MMA issued before
-    // anything this lane issues later.  A tile's page numbers are fetched for
-    // its K copy and again, from L1, for its V copy one step later; with two
+  // One producer lane for the paged and the plain windowed instantiations,
+  // two for the others (measured: one lane is 4-5% faster on windowed calls
+  // and 0.4-0.7% slower on full-causal ones).
+  constexpr bool kOneLane = PAGED || (WIN && !SPL && !SK && !MASK);
+  if (warp == kProdWarp && kOneLane) {
+    // One lane issues Q, K and V in the order the MMA warp consumes them (a
+    // unit's Q, K0, K1, V0, K2, V1, ..., its last V, then the next unit's Q),
+    // so every wait is for a slot freed by an MMA issued before anything this
+    // lane issues later.  Paged KV: a tile's page numbers are fetched for its
+    // K copy and again, from L1, for its V copy one step later; with two
     // lanes of one warp each fetching them, the divergent lanes' dependent
     // loads stalled each other.  (Prefetching the next tile's entries into L1
     // a step ahead measured 17% slower on 16-token pages.)
@@ -792,7 +796,7 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
     }
     __syncwarp();
   }
-  if (warp == kProdWarp && !PAGED) {
+  if (warp == kProdWarp && !kOneLane) {
     if (lane == 0) {
       uint32_t nq = 0, nk[NS];
       for (int s = 0; s < NS; ++s) nk[s] = 0u;
