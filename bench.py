@@ -70,7 +70,7 @@ def load_peaks():
 # The sources that define the roofline kernel (the d=64 single-tile prefill
 # kernel) and its launch: the split-KV merge, the paged and split
 # instantiations and the other head dims do not change it.
-ROOFLINE_KERNEL_SOURCES = ("host.cu", "inst_d64.cu", "launch.h", "prefill_kernel.cuh", "ptx.cuh",
+ROOFLINE_KERNEL_SOURCES = ("host.cu", "inst_d64.cu", "inst_balanced.cu", "launch.h", "prefill_kernel.cuh", "ptx.cuh",
                            "tile_math.cuh")
 
 
@@ -454,13 +454,17 @@ def step_workspace(pkg, mode):
 LONG_PREFIX = 10240
 
 
+def step_uses_balanced(kind, mode, prefix):
+    return (mode == "all" or (mode == "full" and kind == "full_causal")
+            or (mode == "long" and kind == "full_causal" and prefix >= LONG_PREFIX))
+
+
 def step_prepare(pkg, batch, kind, mode, ws, out, lse, stream, prefix=0):
     """A prepared call of the 16k step: the plain entry point, or the
     balanced split for the full-causal calls (`mode` "full"), for the
     full-causal calls over at least LONG_PREFIX cached tokens ("long"), or
     for all calls ("all")."""
-    bal = (mode == "all" or (mode == "full" and kind == "full_causal")
-           or (mode == "long" and kind == "full_causal" and prefix >= LONG_PREFIX))
+    bal = step_uses_balanced(kind, mode, prefix)
     return pkg.prepare(batch, out=out, lse=lse, stream=stream,
                        num_splits=pkg.SPLITS_BALANCED if bal else None,
                        workspace=ws if bal else None)
@@ -558,6 +562,11 @@ def run_oss20b(args, rank, world):
     full_tf = kind_flops["full_causal"] / (kind_ms["full_causal"] * 1e-3) / 1e12
     win_gbs = win_bytes / (kind_ms["window_128"] * 1e-3) / 1e9
     e2e = oss20b_e2e(args, st, metas, calls, out, lse, stream, world, flops, ws)
+    n_bal = sum(1 for cl in calls if cl["kind"] == "full_causal"
+                and step_uses_balanced(cl["kind"], args.balanced, cl["chunk"] * CHUNK))
+    full_kernel_desc = (f"prefill_kernel<64,128,...> full-causal calls ({n_kind['full_causal']} "
+                        f"per step: {n_kind['full_causal'] - n_bal} unsplit, {n_bal} through the "
+                        f"balanced split)")
     del flush
     pair = layer_pair_summary(args, world, peaks)
 
@@ -572,7 +581,7 @@ def run_oss20b(args, rank, world):
         "pct_of_bf16_peak": round(100.0 * value / (world * peaks["bf16_tflops"]), 2),
         "pct_of_bf16_peak_sustained": round(100.0 * value / (world * peaks["bf16_tflops_sustained"]), 2),
         "roofline": {"bound": "tensor",
-                     "kernel": "prefill_kernel<64,128,...> full-causal calls (384 per step)",
+                     "kernel": full_kernel_desc,
                      "achieved": round(full_tf, 2), "peak": peaks["bf16_tflops_sustained"],
                      "unit": "TFLOP/s", "frac": round(full_tf / peaks["bf16_tflops_sustained"], 4),
                      "frac_of_burst": round(full_tf / peaks["bf16_tflops"], 4),
