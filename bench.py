@@ -481,7 +481,8 @@ def run_oss20b(args, rank, world):
     st, metas, calls = oss20b_setup()
     out = torch.empty_like(st.q)
     lse = torch.empty(st.q.shape[:3], dtype=torch.float32, device="cuda")
-    stream = torch.cuda.current_stream()
+    # Everything runs on one side stream: a CUDA graph is captured from it.
+    stream = torch.cuda.Stream()
     L = CHUNK
     ws = step_workspace(pkg, args.balanced)
     for cl in calls:
@@ -496,12 +497,23 @@ def run_oss20b(args, rank, world):
         for cl in calls:
             cl["run"]()
 
-    for _ in range(args.warmup):
-        flush.fill_(1.0)
-        step()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            step()
     torch.cuda.synchronize()
     if pkg.get_device_status() != 0:
         raise RuntimeError("device status word raised during warm-up")
+    # The step's 768 calls as one CUDA graph (their programmatic dependent
+    # launches become programmatic edges), unless --eager: replaying it saves
+    # the per-launch submission cost (1% of the step on GB300).
+    graph = None
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        torch.cuda.synchronize()
+    run_step = graph.replay if graph is not None else step
 
     # Timed region: K steps, each bracketed by events on the launching stream;
     # the L2 flush sits between steps, outside the events.
@@ -511,11 +523,12 @@ def run_oss20b(args, rank, world):
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         t_wall0 = time.perf_counter()
-        for i in range(steps):
-            flush.fill_(float(i))
-            ev[i][0].record(stream)
-            step()
-            ev[i][1].record(stream)
+        with torch.cuda.stream(stream):
+            for i in range(steps):
+                flush.fill_(float(i))
+                ev[i][0].record(stream)
+                run_step()
+                ev[i][1].record(stream)
         torch.cuda.synchronize()
         t_wall1 = time.perf_counter()
         clk.mark(t_wall0, t_wall1)
@@ -533,12 +546,13 @@ def run_oss20b(args, rank, world):
     n_b = max(1, min(steps, 10))
     evb = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
            for _ in range(n_b)]
-    for i in range(n_b):
-        flush.fill_(float(i))
-        evb[i][0].record(stream)
-        for j, cl in enumerate(calls):
-            cl["run"]()
-            evb[i][j + 1].record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(n_b):
+            flush.fill_(float(i))
+            evb[i][0].record(stream)
+            for j, cl in enumerate(calls):
+                cl["run"]()
+                evb[i][j + 1].record(stream)
     torch.cuda.synchronize()
     kind_ms = {"full_causal": 0.0, "window_128": 0.0}
     for i in range(n_b):
@@ -575,7 +589,7 @@ def run_oss20b(args, rank, world):
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) Q/K/V and sinks; no model weights)",
-        "config": bench_config(world, args.balanced),
+        "config": bench_config(world, args.balanced, args.eager),
         "ms_per_step_mean": round(ms_mean, 4),
         "tokens_per_s": round(world * SEQ / (ms_step * 1e-3), 1),
         "pct_of_bf16_peak": round(100.0 * value / (world * peaks["bf16_tflops"]), 2),
@@ -659,7 +673,7 @@ def run_profile(args):
     print(f"profile run done: {n} prefill launches", flush=True)
 
 
-def bench_config(world, balanced="long"):
+def bench_config(world, balanced="long", eager=False):
     entry = {"none": "gqa_flash_prefill",
              "full": "gqa_flash_prefill_splitkv (balanced split) for the full-causal calls, "
                      "gqa_flash_prefill for the window-128 calls",
@@ -670,7 +684,10 @@ def bench_config(world, balanced="long"):
             "layers": LAYERS, "calls_per_step": LAYERS * (SEQ // CHUNK),
             "l2": "inputs larger than L2 (3.8 GB read per step); 256 MiB written between steps",
             "parallelism": "replicas (one per GPU)" if world > 1 else "single GPU",
-            "entry": entry}
+            "entry": entry,
+            "launch": ("each call launched by the host" if eager else
+                       "the step's calls replayed as one CUDA graph, captured once after "
+                       "the warm-up (the e2e object launches them one by one)")}
 
 
 def oss20b_e2e(args, st, metas, calls, out, lse, stream, world, flops, ws=None):
@@ -1190,7 +1207,7 @@ def run_reference(args, rank, world):
             "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) Q/K/V and sinks; no model weights)",
-            "config": bench_config(world, args.balanced),
+            "config": bench_config(world, args.balanced, args.eager),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -1230,6 +1247,9 @@ def main():
                     help="16k prefill: the balanced split (gqa_flash_prefill_splitkv with "
                          "GQA_SPLITS_BALANCED) for no call, the full-causal calls over long "
                          "prefixes, all full-causal calls, or all calls")
+    ap.add_argument("--eager", action="store_true",
+                    help="16k prefill: launch the step's calls one by one instead of replaying "
+                         "them as one CUDA graph")
     ap.add_argument("--profile", choices=["step", "chunk31", "pair"], default=None,
                     help="untimed run for an ncu capture: the warm-up steps plus one step of "
                          "the 16k prefill, chunk 31's two calls, or the layer pair's two "
