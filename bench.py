@@ -449,22 +449,23 @@ def step_workspace(pkg, mode):
     return torch.empty(nbytes, dtype=torch.uint8, device="cuda")
 
 
-# --balanced long: the prefix from which a full-causal chunk call takes the
-# balanced split (measured crossover on GB300: about chunk 20 of 32).
-LONG_PREFIX = 10240
+# --balanced long: the default prefix from which a full-causal chunk call
+# takes the balanced split (--long-prefix changes it).
+LONG_PREFIX = 8192
 
 
-def step_uses_balanced(kind, mode, prefix):
+def step_uses_balanced(kind, mode, prefix, long_prefix=None):
+    lp = LONG_PREFIX if long_prefix is None else long_prefix
     return (mode == "all" or (mode == "full" and kind == "full_causal")
-            or (mode == "long" and kind == "full_causal" and prefix >= LONG_PREFIX))
+            or (mode == "long" and kind == "full_causal" and prefix >= lp))
 
 
-def step_prepare(pkg, batch, kind, mode, ws, out, lse, stream, prefix=0):
+def step_prepare(pkg, batch, kind, mode, ws, out, lse, stream, prefix=0, long_prefix=None):
     """A prepared call of the 16k step: the plain entry point, or the
     balanced split for the full-causal calls (`mode` "full"), for the
-    full-causal calls over at least LONG_PREFIX cached tokens ("long"), or
-    for all calls ("all")."""
-    bal = step_uses_balanced(kind, mode, prefix)
+    full-causal calls over at least `long_prefix` (default LONG_PREFIX)
+    cached tokens ("long"), or for all calls ("all")."""
+    bal = step_uses_balanced(kind, mode, prefix, long_prefix)
     return pkg.prepare(batch, out=out, lse=lse, stream=stream,
                        num_splits=pkg.SPLITS_BALANCED if bal else None,
                        workspace=ws if bal else None)
@@ -489,7 +490,7 @@ def run_oss20b(args, rank, world):
         c, layer = cl["chunk"], cl["layer"]
         cl["run"] = step_prepare(pkg, cl["batch"], cl["kind"], args.balanced, ws,
                                  out[layer, c * L:(c + 1) * L], lse[layer, c * L:(c + 1) * L],
-                                 stream, prefix=c * L)
+                                 stream, prefix=c * L, long_prefix=args.long_prefix)
     flops = sum(cl["flops"] for cl in calls)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
 
@@ -577,7 +578,8 @@ def run_oss20b(args, rank, world):
     win_gbs = win_bytes / (kind_ms["window_128"] * 1e-3) / 1e9
     e2e = oss20b_e2e(args, st, metas, calls, out, lse, stream, world, flops, ws)
     n_bal = sum(1 for cl in calls if cl["kind"] == "full_causal"
-                and step_uses_balanced(cl["kind"], args.balanced, cl["chunk"] * CHUNK))
+                and step_uses_balanced(cl["kind"], args.balanced, cl["chunk"] * CHUNK,
+                                       args.long_prefix))
     full_kernel_desc = (f"prefill_kernel<64,128,...> full-causal calls ({n_kind['full_causal']} "
                         f"per step: {n_kind['full_causal'] - n_bal} unsplit, {n_bal} through the "
                         f"balanced split)")
@@ -589,7 +591,7 @@ def run_oss20b(args, rank, world):
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) Q/K/V and sinks; no model weights)",
-        "config": bench_config(world, args.balanced, args.eager),
+        "config": bench_config(world, args.balanced, args.eager, args.long_prefix),
         "ms_per_step_mean": round(ms_mean, 4),
         "tokens_per_s": round(world * SEQ / (ms_step * 1e-3), 1),
         "pct_of_bf16_peak": round(100.0 * value / (world * peaks["bf16_tflops"]), 2),
@@ -650,7 +652,7 @@ def run_profile(args):
             kind = "window_128" if b.window > 0 else "full_causal"
             step_prepare(pkg, b, kind, args.balanced, ws, torch.empty_like(b.q),
                          torch.empty(b.q.shape[:2], dtype=torch.float32, device="cuda"), stream,
-                         prefix=SEQ - CHUNK)()
+                         prefix=SEQ - CHUNK, long_prefix=args.long_prefix)()
         n = 2
     else:
         st, metas, calls = oss20b_setup()
@@ -661,7 +663,7 @@ def run_profile(args):
         runs = [step_prepare(pkg, cl["batch"], cl["kind"], args.balanced, ws,
                              out[cl["layer"], cl["chunk"] * L:(cl["chunk"] + 1) * L],
                              lse[cl["layer"], cl["chunk"] * L:(cl["chunk"] + 1) * L], stream,
-                             prefix=cl["chunk"] * L)
+                             prefix=cl["chunk"] * L, long_prefix=args.long_prefix)
                 for cl in calls]
         for _ in range(args.warmup + 1):
             for r in runs:
@@ -673,12 +675,13 @@ def run_profile(args):
     print(f"profile run done: {n} prefill launches", flush=True)
 
 
-def bench_config(world, balanced="long", eager=False):
+def bench_config(world, balanced="long", eager=False, long_prefix=None):
+    lp = LONG_PREFIX if long_prefix is None else long_prefix
     entry = {"none": "gqa_flash_prefill",
              "full": "gqa_flash_prefill_splitkv (balanced split) for the full-causal calls, "
                      "gqa_flash_prefill for the window-128 calls",
              "long": f"gqa_flash_prefill_splitkv (balanced split) for the full-causal calls "
-                     f"over >= {LONG_PREFIX} cached tokens, gqa_flash_prefill for the others",
+                     f"over >= {lp} cached tokens, gqa_flash_prefill for the others",
              "all": "gqa_flash_prefill_splitkv (balanced split)"}[balanced]
     return {"workload": WORKLOAD, "global_batch": world, "seq_len": SEQ, "chunk_len": CHUNK,
             "layers": LAYERS, "calls_per_step": LAYERS * (SEQ // CHUNK),
@@ -727,7 +730,8 @@ def oss20b_e2e(args, st, metas, calls, out, lse, stream, world, flops, ws=None):
         runs = [[step_prepare(pkg, s_.call(c, layer, m_[c]),
                               "window_128" if s_.windows[layer] > 0 else "full_causal",
                               args.balanced, ws, o_[layer, c * L:(c + 1) * L],
-                              l_[layer, c * L:(c + 1) * L], stream, prefix=c * L)
+                              l_[layer, c * L:(c + 1) * L], stream, prefix=c * L,
+                              long_prefix=args.long_prefix)
                  for layer in range(n_l)] for c in range(n_c)]
         sets.append({"st": s_, "metas": m_, "out": o_, "lse": l_, "runs": runs,
                      "in_ready": [torch.cuda.Event() for _ in range(n_c)],
@@ -1207,7 +1211,7 @@ def run_reference(args, rank, world):
             "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) Q/K/V and sinks; no model weights)",
-            "config": bench_config(world, args.balanced, args.eager),
+            "config": bench_config(world, args.balanced, args.eager, args.long_prefix),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -1247,6 +1251,9 @@ def main():
                     help="16k prefill: the balanced split (gqa_flash_prefill_splitkv with "
                          "GQA_SPLITS_BALANCED) for no call, the full-causal calls over long "
                          "prefixes, all full-causal calls, or all calls")
+    ap.add_argument("--long-prefix", type=int, default=LONG_PREFIX,
+                    help="--balanced long: cached tokens from which a full-causal call takes "
+                         "the balanced split")
     ap.add_argument("--eager", action="store_true",
                     help="16k prefill: launch the step's calls one by one instead of replaying "
                          "them as one CUDA graph")

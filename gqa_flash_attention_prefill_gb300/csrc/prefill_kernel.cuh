@@ -557,6 +557,22 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // ---------------------------------------------------------------- set-up
+  // A second CTA of a kernel that allocates tensor memory is launched on an
+  // SM only once the resident CTA has relinquished its allocation permit
+  // (measured on GB300: the second wave starts right after it), so an
+  // allocation after the prologue holds each SM's second CTA back by the
+  // prologue's length (about 2.5 us).  The balanced split allocates first:
+  // its shares are equal, so its second wave sets the call's end (chunk 31
+  // of the 16k prefill 139.3 -> 135.9 us).  The other kernels allocate after
+  // the prologue: allocating first made back-to-back full-causal calls 2-3%
+  // slower under programmatic dependent launch (with earlier relinquishing,
+  // the next call's CTAs pair up on the SMs that free first, and the costliest
+  // units are dealt to the lowest CTAs).
+  constexpr bool kEarlyTmem = SK;
+  if (kEarlyTmem && warp == kMmaWarp) {
+    tmem_alloc(smem_u32(misc), kTmemCols);
+    tmem_relinquish();
+  }
   if (tid == 0) {
     for (int i = 0; i < B::kCount; ++i) {
       uint32_t cnt = 1u;
@@ -578,7 +594,14 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
     tma_prefetch_desc(&p.tmap_k);
     tma_prefetch_desc(&p.tmap_v);
   }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  uint32_t tmem = kEarlyTmem ? misc[0] : 0u;
+  // CTAs that end before any MMA hand early-allocated tensor memory back.
+  auto release_tmem = [&]() {
+    if (kEarlyTmem && warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  };
   // Everything above touches only this CTA's own shared memory and the
   // kernel parameters, so under programmatic dependent launch it overlaps
   // the previous kernel's tail.  The next kernel in the stream may start its
@@ -671,6 +694,7 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
       atomicOr(p.status, 2u);  // GQA_DEV_BAD_METADATA
       if (SPL && blockIdx.x == 0) p.part_hdr[0] = 0;  // nothing to merge
     }
+    release_tmem();
     return;
   }
   // Work items: units, times the split count under split-KV.
@@ -712,17 +736,22 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
     }
     fence_proxy_async_smem();  // the rings were written here; TMA writes them next
     __syncthreads();
-    if (sk[2] <= 0) return;  // an empty share (fewer tiles than CTAs)
+    if (sk[2] <= 0) {  // an empty share (fewer tiles than CTAs)
+      release_tmem();
+      return;
+    }
   }
 
-  if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(misc), kTmemCols);
-    tmem_relinquish();
+  if constexpr (!kEarlyTmem) {
+    if (warp == kMmaWarp) {
+      tmem_alloc(smem_u32(misc), kTmemCols);
+      tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    tmem = misc[0];
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = misc[0];
 
   // ---------------------------------------------------------------- producer
   // Two lanes of the producer warp, each with its own bounded waits: lane 0
