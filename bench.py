@@ -480,6 +480,10 @@ def run_oss20b(args, rank, world):
     torch.cuda.set_device(local)
     pkg.load()
     st, metas, calls = oss20b_setup()
+    # The chunks' metadata is uploaded once, before any call (and, in the e2e
+    # object, by copies the compute stream waits for): no kernel writes it, so
+    # the kernels may read it before waiting on the previous kernel.
+    pkg.set_call_flags(0 if args.no_metadata_ready else pkg.FLAG_METADATA_READY)
     out = torch.empty_like(st.q)
     lse = torch.empty(st.q.shape[:3], dtype=torch.float32, device="cuda")
     # Everything runs on one side stream: a CUDA graph is captured from it.
@@ -591,7 +595,8 @@ def run_oss20b(args, rank, world):
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) Q/K/V and sinks; no model weights)",
-        "config": bench_config(world, args.balanced, args.eager, args.long_prefix),
+        "config": bench_config(world, args.balanced, args.eager, args.long_prefix,
+                               not args.no_metadata_ready),
         "ms_per_step_mean": round(ms_mean, 4),
         "tokens_per_s": round(world * SEQ / (ms_step * 1e-3), 1),
         "pct_of_bf16_peak": round(100.0 * value / (world * peaks["bf16_tflops"]), 2),
@@ -639,6 +644,7 @@ def run_profile(args):
     from gqa_flash_attention_prefill_gb300 import workloads as W
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     pkg.load()
+    pkg.set_call_flags(0 if args.no_metadata_ready else pkg.FLAG_METADATA_READY)
     stream = torch.cuda.current_stream()
     if args.profile == "pair":
         for b in W.layer_pair(seq=4096, seed=1):
@@ -675,7 +681,7 @@ def run_profile(args):
     print(f"profile run done: {n} prefill launches", flush=True)
 
 
-def bench_config(world, balanced="long", eager=False, long_prefix=None):
+def bench_config(world, balanced="long", eager=False, long_prefix=None, metadata_ready=True):
     lp = LONG_PREFIX if long_prefix is None else long_prefix
     entry = {"none": "gqa_flash_prefill",
              "full": "gqa_flash_prefill_splitkv (balanced split) for the full-causal calls, "
@@ -690,7 +696,10 @@ def bench_config(world, balanced="long", eager=False, long_prefix=None):
             "entry": entry,
             "launch": ("each call launched by the host" if eager else
                        "the step's calls replayed as one CUDA graph, captured once after "
-                       "the warm-up (the e2e object launches them one by one)")}
+                       "the warm-up (the e2e object launches them one by one)"),
+            "call_flags": ("GQA_FLAG_METADATA_READY (metadata uploaded once per chunk, "
+                           "read before the kernel waits on its predecessor)"
+                           if metadata_ready else "none")}
 
 
 def oss20b_e2e(args, st, metas, calls, out, lse, stream, world, flops, ws=None):
@@ -1211,7 +1220,8 @@ def run_reference(args, rank, world):
             "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) Q/K/V and sinks; no model weights)",
-            "config": bench_config(world, args.balanced, args.eager, args.long_prefix),
+            "config": bench_config(world, args.balanced, args.eager, args.long_prefix,
+                               not args.no_metadata_ready),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -1254,6 +1264,9 @@ def main():
     ap.add_argument("--long-prefix", type=int, default=LONG_PREFIX,
                     help="--balanced long: cached tokens from which a full-causal call takes "
                          "the balanced split")
+    ap.add_argument("--no-metadata-ready", action="store_true",
+                    help="16k prefill: do not set GQA_FLAG_METADATA_READY (the kernels then "
+                         "read the metadata only after waiting on the previous kernel)")
     ap.add_argument("--eager", action="store_true",
                     help="16k prefill: launch the step's calls one by one instead of replaying "
                          "them as one CUDA graph")

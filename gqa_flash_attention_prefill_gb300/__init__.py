@@ -21,12 +21,14 @@ __all__ = ["load", "gqa_flash_prefill", "gqa_flash_prefill_debug", "prefill", "p
            "NOALLOC_SCRATCH_BYTES", "gqa_flash_prefill_paged", "prefill_paged",
            "clear_config_cache", "config_block_n", "selftest_timeout", "GQAError",
            "GQA_F16", "GQA_BF16", "GQA_DEV_TIMEOUT", "GQA_DEV_BAD_METADATA", "SPLITS_BALANCED",
+           "FLAG_METADATA_READY", "set_call_flags", "get_call_flags",
            "EXPORTED_SYMBOLS"]
 
 GQA_F16, GQA_BF16 = 0, 1
 GQA_OK, GQA_ERR_INVALID, GQA_ERR_UNSUPPORTED, GQA_ERR_CUDA = 0, -1, -2, -3
 GQA_DEV_TIMEOUT, GQA_DEV_BAD_METADATA = 1, 2
 SPLITS_BALANCED = -1  # num_splits of the balanced split (GQA_SPLITS_BALANCED)
+FLAG_METADATA_READY = 1  # GQA_FLAG_METADATA_READY (gqa_prefill_set_call_flags)
 
 EXPORTED_SYMBOLS = [
     "gqa_flash_prefill", "gqa_flash_prefill_debug", "gqa_prefill_plan",
@@ -37,6 +39,7 @@ EXPORTED_SYMBOLS = [
     "gqa_flash_prefill_splitkv", "gqa_prefill_splitkv_workspace",
     "gqa_flash_prefill_splitkv_noalloc", "gqa_flash_prefill_paged",
     "gqa_prefill_get_stream_status", "gqa_flash_prefill_masked",
+    "gqa_prefill_set_call_flags", "gqa_prefill_get_call_flags",
 ]
 NOALLOC_SCRATCH_BYTES = 32 << 20  # the library's file-scope split-KV scratch (gqa_prefill.h)
 
@@ -116,6 +119,10 @@ def load(path: Optional[str] = None):
     lib.gqa_prefill_selftest_timeout.argtypes = [ctypes.c_int, ctypes.c_void_p,
                                                  ctypes.POINTER(ctypes.c_int)]
     lib.gqa_prefill_selftest_timeout.restype = ctypes.c_int
+    lib.gqa_prefill_set_call_flags.argtypes = [ctypes.c_uint]
+    lib.gqa_prefill_set_call_flags.restype = ctypes.c_int
+    lib.gqa_prefill_get_call_flags.argtypes = []
+    lib.gqa_prefill_get_call_flags.restype = ctypes.c_uint
     if path is None:
         _lib = lib
     return lib
@@ -400,6 +407,18 @@ def prepare(batch, out, lse=None, stream=None, num_splits=None, workspace=None) 
     ``out`` (and ``lse`` when given) on ``stream``; with ``num_splits`` (for
     example SPLITS_BALANCED) the split-KV entry point on ``workspace``."""
     return PreparedCall(batch, out, lse, stream, num_splits, workspace)
+
+
+def set_call_flags(flags: int) -> None:
+    """Flags for the calling thread's later calls (gqa_prefill_set_call_flags):
+    FLAG_METADATA_READY, or 0."""
+    rc = load().gqa_prefill_set_call_flags(int(flags))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_prefill_set_call_flags")
+
+
+def get_call_flags() -> int:
+    return int(load().gqa_prefill_get_call_flags())
 
 
 def plan(num_seqs, total_q, max_seqlen_q, hq, hkv, d, dtype, window) -> dict:

@@ -49,6 +49,9 @@ __global__ void selftest_wait_kernel(unsigned int* status, unsigned long long ti
 
 namespace {
 
+// Per-host-thread call flags (gqa_prefill_set_call_flags), read at each launch.
+thread_local unsigned int t_call_flags = 0u;
+
 std::mutex g_mu;      // guards the configuration cache and the forced variant
 std::mutex g_dev_mu;  // guards the per-device information
 int g_forced_block_n = 0;
@@ -495,6 +498,7 @@ int launch_planned(const Plan& pl, const void* q, const void* k, const void* v,
   p.part_hdr = sp.part_hdr;
   p.sk_count = sp.sk_count;
   p.epoch = sp.balanced ? next_epoch() : 0ull;
+  p.metadata_ready = (t_call_flags & GQA_FLAG_METADATA_READY) ? 1 : 0;
   int grid = pl.grid;
   if (p.num_splits > 1) {  // more work items than units: fill the resident slots
     const long long items = (long long)pl.max_units * p.num_splits;
@@ -1086,6 +1090,14 @@ int gqa_prefill_get_stream_status(void* stream, int* status) {
   *status = (int)v;
   return GQA_OK;
 }
+
+int gqa_prefill_set_call_flags(unsigned int flags) {
+  if ((flags & ~GQA_FLAG_METADATA_READY) != 0u) return GQA_ERR_INVALID;
+  gqa::t_call_flags = flags;
+  return GQA_OK;
+}
+
+unsigned int gqa_prefill_get_call_flags(void) { return gqa::t_call_flags; }
 
 const char* gqa_prefill_status_string(int code) {
   switch (code) {

@@ -100,6 +100,10 @@ struct PrefillParams {
   // the launch's epoch in their upper 48 bits, so stale words count as zero.
   unsigned long long* sk_count;
   unsigned long long epoch;
+  // The caller declared the metadata arrays (cu_seqlens_q, prefix_lens,
+  // kv_indptr, mask_indptr) ready before this kernel starts: the prologue
+  // reads them before waiting on the previous kernel in the stream.
+  int metadata_ready;
 };
 
 __host__ __device__ constexpr int pow2_cols(int n) {
@@ -605,10 +609,12 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
   // Everything above touches only this CTA's own shared memory and the
   // kernel parameters, so under programmatic dependent launch it overlaps
   // the previous kernel's tail.  The next kernel in the stream may start its
-  // own set-up as soon as this grid's CTAs finish; nothing below reads
-  // device memory before the previous kernel's writes are visible.
+  // own set-up as soon as this grid's CTAs finish.  Nothing reads device
+  // memory before the previous kernel's writes are visible, except, when the
+  // caller declares them ready (metadata_ready), the metadata arrays the
+  // prologue below reads; no global write comes before the wait either way.
   grid_dep_launch_dependents();
-  grid_dep_wait();
+  if (!p.metadata_ready) grid_dep_wait();
 
   // Per-sequence tables and metadata checks (bad metadata: write nothing,
   // raise GQA_DEV_BAD_METADATA), the order in which sequences are dealt, and
@@ -689,7 +695,69 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
     }
   }
   __syncthreads();
-  if (misc[2] != 0u) {
+  // This CTA's work, still from shared memory only: the units (times the
+  // split count under split-KV), whether the CTA has any, the balanced
+  // split's share, and the tensor memory.  With metadata_ready all of it
+  // runs before the wait on the previous kernel, so each SM's second CTA is
+  // not held back by the wait (it starts once this one has relinquished its
+  // tensor-memory allocation permit).  Global writes (the bad-metadata
+  // report, the split-KV header) come after the wait.
+  const bool bad_meta = misc[2] != 0u;
+  const int n_units = tile_start[nseq] * p.Hkv * (SPL ? p.num_splits : 1);
+  bool run = !bad_meta && (SK || (int)blockIdx.x < n_units);
+  // Balanced split: the key tiles of every query tile (in dealing order) into
+  // the K/V rings, still unused, their exclusive scan, and this CTA's share:
+  // sk[0] first unit, sk[1] its first tile, sk[2] tiles, sk[3] global index of
+  // the first tile, sk[4] W (the host keeps W below 2^31 and the query tiles
+  // within the rings).  Skipped on bad metadata, whose counts are not bounded.
+  int32_t* const sk = scan + 8;
+  if constexpr (SK) {
+    static_assert(kThr / 32 <= 8, "scan words 8..12 hold the share");
+    if (run) {
+      int32_t* qn = reinterpret_cast<int32_t*>(smem + NQ * QT * kQBytes);
+      const int nq = tile_start[nseq];
+      for (int q = tid; q < nq; q += kThr) qn[q] = decode_unit(p, T, q * p.Hkv, BN, urows).n_tiles;
+      __syncthreads();
+      cta_exclusive_scan(qn, nq, scan, tid, kThr);
+      if (tid == 0) {
+        const int W = p.Hkv * qn[nq], c = blockIdx.x;
+        const SkShares sh(W, (int)gridDim.x);
+        const int lo = sh.lo(c), hi = sh.lo(c + 1);
+        sk[0] = 0;
+        sk[1] = 0;
+        if (hi > lo) {  // query tile holding global tile lo: Hkv qn[a] <= lo < Hkv qn[a + 1]
+          int a = 0, b = nq;
+          while (b - a > 1) {
+            const int mid = (a + b) >> 1;
+            if (p.Hkv * qn[mid] <= lo) a = mid; else b = mid;
+          }
+          const int off = lo - p.Hkv * qn[a], n = qn[a + 1] - qn[a];  // n >= 1
+          sk[0] = a * p.Hkv + off / n;
+          sk[1] = off % n;
+        }
+        sk[2] = hi - lo;
+        sk[3] = lo;
+        sk[4] = W;
+      }
+      fence_proxy_async_smem();  // the rings were written here; TMA writes them next
+      __syncthreads();
+      run = sk[2] > 0;  // false: an empty share (fewer tiles than CTAs)
+    }
+  }
+  if constexpr (!kEarlyTmem) {
+    if (run) {
+      if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(misc), kTmemCols);
+        tmem_relinquish();
+      }
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      tmem = misc[0];
+    }
+  }
+  if (p.metadata_ready) grid_dep_wait();  // before the first global write or other read
+  if (bad_meta) {
     if (tid == 0) {
       atomicOr(p.status, 2u);  // GQA_DEV_BAD_METADATA
       if (SPL && blockIdx.x == 0) p.part_hdr[0] = 0;  // nothing to merge
@@ -697,60 +765,10 @@ __global__ void __launch_bounds__(threads_for(QT), MINB)
     release_tmem();
     return;
   }
-  // Work items: units, times the split count under split-KV.
-  const int n_units = tile_start[nseq] * p.Hkv * (SPL ? p.num_splits : 1);
   if (SPL && blockIdx.x == 0 && tid == 0) p.part_hdr[0] = tile_start[nseq] * p.Hkv;
-  if (!SK && blockIdx.x >= n_units) return;  // nothing for this CTA (before any TMEM use)
-  // Balanced split: the key tiles of every query tile (in dealing order) into
-  // the K/V rings, still unused, their exclusive scan, and this CTA's share:
-  // sk[0] first unit, sk[1] its first tile, sk[2] tiles, sk[3] global index of
-  // the first tile, sk[4] W (the host keeps W below 2^31 and the query tiles
-  // within the rings).
-  int32_t* const sk = scan + 8;
-  if constexpr (SK) {
-    static_assert(kThr / 32 <= 8, "scan words 8..12 hold the share");
-    int32_t* qn = reinterpret_cast<int32_t*>(smem + NQ * QT * kQBytes);
-    const int nq = tile_start[nseq];
-    for (int q = tid; q < nq; q += kThr) qn[q] = decode_unit(p, T, q * p.Hkv, BN, urows).n_tiles;
-    __syncthreads();
-    cta_exclusive_scan(qn, nq, scan, tid, kThr);
-    if (tid == 0) {
-      const int W = p.Hkv * qn[nq], c = blockIdx.x;
-      const SkShares sh(W, (int)gridDim.x);
-      const int lo = sh.lo(c), hi = sh.lo(c + 1);
-      sk[0] = 0;
-      sk[1] = 0;
-      if (hi > lo) {  // query tile holding global tile lo: Hkv qn[a] <= lo < Hkv qn[a + 1]
-        int a = 0, b = nq;
-        while (b - a > 1) {
-          const int mid = (a + b) >> 1;
-          if (p.Hkv * qn[mid] <= lo) a = mid; else b = mid;
-        }
-        const int off = lo - p.Hkv * qn[a], n = qn[a + 1] - qn[a];  // n >= 1
-        sk[0] = a * p.Hkv + off / n;
-        sk[1] = off % n;
-      }
-      sk[2] = hi - lo;
-      sk[3] = lo;
-      sk[4] = W;
-    }
-    fence_proxy_async_smem();  // the rings were written here; TMA writes them next
-    __syncthreads();
-    if (sk[2] <= 0) {  // an empty share (fewer tiles than CTAs)
-      release_tmem();
-      return;
-    }
-  }
-
-  if constexpr (!kEarlyTmem) {
-    if (warp == kMmaWarp) {
-      tmem_alloc(smem_u32(misc), kTmemCols);
-      tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    tmem = misc[0];
+  if (!run) {  // nothing for this CTA
+    release_tmem();
+    return;
   }
 
   // ---------------------------------------------------------------- producer

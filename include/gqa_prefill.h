@@ -420,6 +420,34 @@ GQA_API int gqa_prefill_get_device_status(int* status);
  */
 GQA_API int gqa_prefill_get_stream_status(void* stream, int* status);
 
+/* Call flag: the metadata arrays are ready (see gqa_prefill_set_call_flags). */
+#define GQA_FLAG_METADATA_READY 1u
+
+/*
+ * Flags for the prefill calls made later by the calling host thread (until
+ * changed; 0 at thread start).  Not an operation of the pages: a launch
+ * detail of this library.
+ *
+ * GQA_FLAG_METADATA_READY: the caller guarantees that the metadata arrays a
+ * call reads (cu_seqlens_q, prefix_lens, kv_indptr or kv_page_indptr,
+ * mask_indptr) are not written by any kernel that may still be running when
+ * the call's kernel starts, for example because they were uploaded once per
+ * batch, before the layers' kernels.  The kernels are launched with
+ * programmatic dependent launch and may start while the previous kernel in
+ * the stream finishes: with this flag, a kernel reads and checks the
+ * metadata and plans its work before it waits for that kernel, instead of
+ * after (measured on the 16k prefill step: 2.4% faster).  Everything else
+ * (q, k, v, page tables, masks, sinks) is still read after the wait, and
+ * nothing is written before it.  Breaking the guarantee can give wrong
+ * results without any error.
+ *
+ * Returns GQA_OK, or GQA_ERR_INVALID for unknown flag bits (flags unchanged).
+ */
+GQA_API int gqa_prefill_set_call_flags(unsigned int flags);
+
+/* The calling host thread's call flags. */
+GQA_API unsigned int gqa_prefill_get_call_flags(void);
+
 /* Static text for a GQA_* return code. */
 GQA_API const char* gqa_prefill_status_string(int code);
 

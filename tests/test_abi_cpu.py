@@ -233,3 +233,23 @@ def _call_masked(lib, **over):
 ])
 def test_masked_entry_validates_before_launch(lib, over, code):
     assert _call_masked(lib, **over) == code
+
+
+def test_call_flags_are_per_thread_and_checked(lib):
+    """gqa_prefill_set_call_flags: known bits only, and the flags belong to
+    the calling host thread (another thread starts at 0)."""
+    import threading
+    import gqa_flash_attention_prefill_gb300 as pkg
+    assert lib.gqa_prefill_get_call_flags() == 0
+    assert lib.gqa_prefill_set_call_flags(2) == -1
+    assert lib.gqa_prefill_set_call_flags(pkg.FLAG_METADATA_READY) == 0
+    try:
+        assert lib.gqa_prefill_get_call_flags() == pkg.FLAG_METADATA_READY
+        seen = []
+        t = threading.Thread(target=lambda: seen.append(lib.gqa_prefill_get_call_flags()))
+        t.start()
+        t.join()
+        assert seen == [0]
+    finally:
+        assert lib.gqa_prefill_set_call_flags(0) == 0
+    assert lib.gqa_prefill_get_call_flags() == 0
