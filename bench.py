@@ -451,7 +451,7 @@ def step_workspace(pkg, mode):
 
 # --balanced long: the default prefix from which a full-causal chunk call
 # takes the balanced split (--long-prefix changes it).
-LONG_PREFIX = 8192
+LONG_PREFIX = 6144
 
 
 def step_uses_balanced(kind, mode, prefix, long_prefix=None):
